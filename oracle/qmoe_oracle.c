@@ -1,0 +1,258 @@
+/*
+ * CPU oracle for the NVFP4 W4A16 mixture-of-experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the layer computes, in fp64.  Only the tests, the smoke check
+ * and the benchmark's CPU-baseline / reference arm may load it.  It shares no code,
+ * header, table or helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * Sources (the NVFP4 MoE pages):
+ *  - megamoe_rm.cu (sm121 W4A16 NVFP4 MoE forward): header comment (w13 rows
+ *    0..I-1 are up and I..2I-1 gate; w2 is [H][I/2]; global scale multiplies the
+ *    accumulator), route_prep (a pair's slot is its rank among earlier pairs with
+ *    the same expert; expert -1 is skipped), fc1_rm epilogue (SiLU(gate)*up, h
+ *    rounded to a 16-bit type), fc2_rm epilogue (global scale times routing weight
+ *    times accumulator, written per (token, k) pair), combine (sum over k in k
+ *    order, skipping pairs without an expert, rounded to bf16).
+ *  - tilelang_kernels.py (grouped_gemm_fp4): per-expert dequantize-then-linear
+ *    and the routing-weighted sum over the top-k slots.
+ *  - cutlass discussion 2855: per-expert row offsets ("total tokens including
+ *    expert") as the grouping of the rows.
+ *
+ * Readings where the pages leave a step open (all listed in the design notes):
+ *  - E2M1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}, sign in bit 3; the even K
+ *    element sits in the low nibble of its byte.
+ *  - E4M3: sign bit 7, exponent bits 6..3 with bias 7, mantissa bits 2..0,
+ *    exponent 0 is subnormal (m/8 * 2^-6), 0x7F / 0xFF are NaN (rejected), no
+ *    infinities.  Scales may be negative; they are decoded as general E4M3.
+ *  - h is rounded to bf16 (round to nearest, ties to even) after SiLU(gate)*up;
+ *    every other intermediate stays fp64; the layer output is rounded to bf16.
+ *  - SiLU(g) = g / (1 + exp(-g)).
+ *  - Expert ids < 0 contribute nothing; ids >= E are invalid: they are skipped
+ *    like -1 and the call returns QO_WARN_BAD_ID.
+ *  - Routing weights are used as given (no renormalisation); a token may name the
+ *    same expert in several slots, each slot is its own pair.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define QO_OK 0
+#define QO_ERR_ARG -1
+#define QO_ERR_NAN_SCALE -2
+#define QO_WARN_BAD_ID 1
+
+/* E2M1: sign bit 3; magnitude code 0..7 -> {0, .5, 1, 1.5, 2, 3, 4, 6}. */
+static const double kE2M1Mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double qo_dec_e2m1(int code) {
+  double m = kE2M1Mag[code & 7];
+  return (code & 8) ? -m : m;
+}
+
+/* E4M3 ("fn" variant, the block-scale format): decoded from its bit fields. */
+double qo_dec_e4m3(int b) {
+  b &= 0xFF;
+  int s = (b >> 7) & 1;
+  int e = (b >> 3) & 0xF;
+  int m = b & 7;
+  double v;
+  if (e == 0xF && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* bf16 <-> double.  Rounding goes straight from double to bf16 (8 significant
+ * bits, ties to even), never through fp32. */
+double qo_bf16_to_double(uint16_t b) {
+  int s = (b >> 15) & 1;
+  int e = (b >> 7) & 0xFF;
+  int m = b & 0x7F;
+  double v;
+  if (e == 0xFF) return m ? NAN : (s ? -INFINITY : INFINITY);
+  if (e == 0)
+    v = ldexp((double)m, -133);
+  else
+    v = ldexp(1.0 + (double)m / 128.0, e - 127);
+  return s ? -v : v;
+}
+
+uint16_t qo_bf16_rne(double v) {
+  if (isnan(v)) return 0x7FC0;
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+  int ex;
+  frexp(a, &ex);      /* a in [2^(ex-1), 2^ex) */
+  int e = ex - 1;
+  if (e < -126) e = -126; /* subnormal range keeps the quantum 2^-133 */
+  double q = ldexp(1.0, e - 7);
+  double r = rint(a / q) * q; /* default rounding mode: nearest, ties to even */
+  if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+  if (r < ldexp(1.0, -126)) return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -133)));
+  int ex2;
+  double f = frexp(r, &ex2); /* r = f * 2^ex2, f in [0.5, 1) */
+  int E = ex2 - 1;
+  uint16_t mant = (uint16_t)((f * 2.0 - 1.0) * 128.0);
+  return (uint16_t)(sign | ((E + 127) << 7) | mant);
+}
+
+/*
+ * Expert grouping (megamoe_rm.cu route_prep; cutlass discussion 2855 offsets).
+ * ids[P] with P = M * top_k, pair index i = token * top_k + k.
+ *   offsets[e]       = number of valid pairs with expert < e, offsets[E] = total
+ *   sorted_pair[pos] = the pair at position pos of the expert-major, stable order
+ *                      (a pair's rank within its expert = number of earlier pairs
+ *                      with the same expert); entries past offsets[E] are -1
+ *   pair_pos[i]      = inverse permutation, -1 for skipped pairs
+ *   tiles[t]         = (expert, start position, rows <= tile_n), experts ascending,
+ *                      positions ascending within an expert; *n_tiles = count
+ * tiles must hold ceil(P / tile_n) + E triples.
+ */
+int qo_route(const int32_t* ids, int64_t P, int E, int tile_n, int32_t* offsets,
+             int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles) {
+  if (P < 0 || E < 1 || tile_n < 1) return QO_ERR_ARG;
+  int bad = 0;
+  int64_t* count = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+  int64_t* seen = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+  if (!count || !seen) { free(count); free(seen); return QO_ERR_ARG; }
+  for (int64_t i = 0; i < P; ++i) {
+    int e = ids[i];
+    if (e >= E) bad = 1;
+    if (e >= 0 && e < E) count[e] += 1;
+  }
+  int64_t run = 0;
+  for (int e = 0; e < E; ++e) {
+    offsets[e] = (int32_t)run;
+    run += count[e];
+  }
+  offsets[E] = (int32_t)run;
+  for (int64_t pos = 0; pos < P; ++pos) sorted_pair[pos] = -1;
+  for (int64_t i = 0; i < P; ++i) {
+    int e = ids[i];
+    if (e < 0 || e >= E) {
+      pair_pos[i] = -1;
+      continue;
+    }
+    int64_t pos = offsets[e] + seen[e];
+    seen[e] += 1;
+    sorted_pair[pos] = (int32_t)i;
+    pair_pos[i] = (int32_t)pos;
+  }
+  int32_t t = 0;
+  for (int e = 0; e < E; ++e) {
+    for (int64_t start = offsets[e]; start < offsets[e + 1]; start += tile_n) {
+      int64_t rows = offsets[e + 1] - start;
+      if (rows > tile_n) rows = tile_n;
+      tiles[3 * t + 0] = e;
+      tiles[3 * t + 1] = (int32_t)start;
+      tiles[3 * t + 2] = (int32_t)rows;
+      t += 1;
+    }
+  }
+  *n_tiles = t;
+  free(count);
+  free(seen);
+  return bad ? QO_WARN_BAD_ID : QO_OK;
+}
+
+/* One dequantized weight: code (nibble) times its 16-element block's E4M3 scale. */
+static double wq(const uint8_t* w, const uint8_t* s, int64_t K, int64_t n, int64_t k) {
+  uint8_t byte = w[n * (K / 2) + k / 2];
+  int code = (k & 1) ? (byte >> 4) : (byte & 0xF);
+  return qo_dec_e2m1(code) * qo_dec_e4m3(s[n * (K / 16) + k / 16]);
+}
+
+/*
+ * The layer for a subset of tokens (all of them when tokens == NULL):
+ *   for each slot k of token m with expert e = ids[m][k] in [0, E):
+ *     g[n]  = gs13[e] * sum_h x[m][h] * Wq13[e][n][h]        n < 2I
+ *     h[i]  = bf16( silu(g[I + i]) * g[i] )                   i < I (up = rows < I)
+ *     y[j]  = gs2[e] * sum_i h[i] * Wq2[e][j][i]              j < H
+ *   out[m][j] = bf16( sum over k ascending of topk_w[m][k] * y_k[j] )
+ * x is bf16 bits [M][H]; weights are the plain row-major NVFP4 tensors
+ * w13 [E][2I][H/2], s13 [E][2I][H/16], w2 [E][H][I/2], s2 [E][H][I/16].
+ * out_bf16 / out_f64 are [n_tokens][H] (out_f64 may be NULL).
+ */
+int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
+               const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
+               const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
+               const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
+               int nthreads) {
+  if (M < 0 || H < 16 || I < 16 || H % 16 || I % 16 || E < 1 || top_k < 1) return QO_ERR_ARG;
+  if (tokens == NULL) n_tokens = M;
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    int64_t m = tokens ? tokens[t] : t;
+    if (m < 0 || m >= M) return QO_ERR_ARG;
+  }
+  int bad_id = 0, nan_scale = 0;
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* g = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* h = (double*)malloc(sizeof(double) * (size_t)I);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n_tokens; ++t) {
+      int64_t m = tokens ? tokens[t] : t;
+      for (int64_t j = 0; j < H; ++j) acc[j] = 0.0;
+      for (int k = 0; k < top_k; ++k) {
+        int e = ids[m * top_k + k];
+        if (e < 0) continue;
+        if (e >= E) {
+          bad_id = 1;
+          continue;
+        }
+        const uint8_t* we = w13 + (int64_t)e * (2 * I) * (H / 2);
+        const uint8_t* se = s13 + (int64_t)e * (2 * I) * (H / 16);
+        for (int64_t n = 0; n < 2 * I; ++n) {
+          double sum = 0.0;
+          for (int64_t hh = 0; hh < H; ++hh)
+            sum += qo_bf16_to_double(x[m * H + hh]) * wq(we, se, H, n, hh);
+          g[n] = (double)gs13[e] * sum;
+        }
+        for (int64_t i = 0; i < I; ++i) {
+          double up = g[i], gate = g[I + i];
+          double silu = gate / (1.0 + exp(-gate));
+          h[i] = qo_bf16_to_double(qo_bf16_rne(silu * up));
+        }
+        const uint8_t* w2e = w2 + (int64_t)e * H * (I / 2);
+        const uint8_t* s2e = s2 + (int64_t)e * H * (I / 16);
+        for (int64_t j = 0; j < H; ++j) {
+          double sum = 0.0;
+          for (int64_t i = 0; i < I; ++i) sum += h[i] * wq(w2e, s2e, I, j, i);
+          double y = (double)gs2[e] * sum;
+          acc[j] += (double)topk_w[m * top_k + k] * y;
+        }
+      }
+      for (int64_t j = 0; j < H; ++j) {
+        if (isnan(acc[j])) nan_scale = 1; /* a NaN scale (or input) reached the output */
+        out_bf16[t * H + j] = qo_bf16_rne(acc[j]);
+        if (out_f64) out_f64[t * H + j] = acc[j];
+      }
+    }
+    free(g);
+    free(h);
+    free(acc);
+  }
+  if (nan_scale) return QO_ERR_NAN_SCALE;
+  return bad_id ? QO_WARN_BAD_ID : QO_OK;
+}
+
+/* Number of threads OpenMP would use by default (the host's cores). */
+int qo_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
