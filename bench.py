@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 W4A16 MoE layer (route -> FC1 + SwiGLU -> FC2 -> combine).
+
+One step = one pass of the whole layer over one batch: moe_nvfp4_forward through the
+C-ABI (route, gather, FC1, FC2, combine).  Default workload: DeepSeek-class decode,
+M=16 tokens, H=7168, I=2048, E=256 experts, top_k=8, synthetic seeded inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+Prints one JSON line on rank 0.  Under torchrun (N > 1) every rank runs its own batch
+(weak scaling, no collective on the data path); value = all ranks' tokens / max time.
+The reference arm times the CPU oracle on the host cores on a bounded sample of the
+same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "decode_m16_h7168_i2048_e256_k8"
+METRIC = "MoE layer tokens/s (decode M=16, H=7168, I=2048, E=256, top_k=8, NVFP4 W4A16)"
+STAGES = ["route", "gather", "fc1", "fc2", "combine"]
+KERNEL_SOURCES = ["csrc/gemm.cu", "csrc/dequant.cuh", "csrc/common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--sched", choices=["auto", "decode", "prefill"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained",
+                                                                           d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "quantized_moe_grouped_route_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources still
+    match the ones that were profiled; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(f"{kernel}:{workload}")
+    if not ent or ent.get("source_sha") != kernel_source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(cfg, ids_cpu):
+    """Per-launch algorithmic DRAM bytes of FC1 and FC2 and the layer's weight bytes."""
+    import numpy as np
+    ids = ids_cpu.numpy().reshape(-1)
+    valid = ids[(ids >= 0) & (ids < cfg.E)]
+    touched = int(np.unique(valid).size)
+    n_valid = int(valid.size)
+    H, I = cfg.H, cfg.I
+    w13 = touched * (2 * I * H * (0.5 + 1 / 16) + 4)
+    w2 = touched * (H * I * (0.5 + 1 / 16) + 4)
+    fc1 = w13 + n_valid * H * 2 + n_valid * I * 2          # weights + gathered x + h
+    fc2 = w2 + n_valid * I * 2 + n_valid * H * 4           # weights + h + fp32 partials
+    return {"touched_experts": touched, "pairs": n_valid, "fc1": fc1, "fc2": fc2,
+            "weights": w13 + w2, "flops": 2.0 * n_valid * 3 * H * I}
+
+
+def run_cpu_oracle(li, n_tokens: int):
+    """Time the CPU oracle on the first n_tokens tokens; returns (tokens/s, seconds, threads)."""
+    import oracle
+    toks = list(range(min(n_tokens, li.cfg.M)))
+    threads = oracle.max_threads()
+    host = [t.detach().cpu() for t in (li.x, li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2,
+                                       li.topk_ids, li.topk_weights)]
+    t0 = time.perf_counter()
+    oracle.forward(*host, tokens=toks, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return len(toks) / dt, dt, threads, len(toks)
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    import torch
+
+    from qmoe_inputs import config_by_name, make_inputs
+    import oracle
+    cfg = config_by_name(args.config)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    li = make_inputs(cfg, dev)
+    threads = oracle.max_threads()
+    n_tok = max(1, min(cfg.M, threads))
+    for _ in range(max(args.warmup, 0)):
+        run_cpu_oracle(li, n_tok)
+    times = []
+    for _ in range(args.steps):
+        _, dt, threads, n = run_cpu_oracle(li, n_tok)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps * n_tok / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "M": cfg.M, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                   "top_k": cfg.top_k},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_tok} of {cfg.M} tokens per step (all their top_k slots)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def ours_arm(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_moe_grouped_route_gb300 import NVFP4MoE, qmoe
+    from qmoe_inputs import config_by_name, make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = config_by_name(args.config)
+    sched = {"auto": qmoe.QMOE_SCHED_AUTO, "decode": qmoe.QMOE_SCHED_DECODE,
+             "prefill": qmoe.QMOE_SCHED_PREFILL}[args.sched]
+    li = make_inputs(cfg, dev, token_seed=cfg.seed + 1000 * rank)
+    torch.cuda.synchronize()
+
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record()
+    layer = NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
+    r1.record()
+    torch.cuda.synchronize()
+    repack_ms = r0.elapsed_time(r1)
+
+    M, H, I, E, top_k = cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k
+    ws = layer.workspace(M, top_k, sched, dev)
+    out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        if events is None:
+            qmoe.moe_nvfp4_forward(li.x, layer.w13c, layer.w13s, layer.gs13, layer.w2c, layer.w2s,
+                                   layer.gs2, li.topk_ids, li.topk_weights, out, H=H, I=I, E=E,
+                                   sched=sched, workspace=ws, stream=stream)
+        else:
+            qmoe.moe_nvfp4_forward_events(li.x, layer.w13c, layer.w13s, layer.gs13, layer.w2c,
+                                          layer.w2s, layer.gs2, li.topk_ids, li.topk_weights, out,
+                                          events, H=H, I=I, E=E, sched=sched, workspace=ws,
+                                          stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    rc, flags = qmoe.qmoe_read_error(ws)
+    if rc != 0:
+        raise RuntimeError(f"device error word after warm-up: rc={rc} flags={flags}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_soak = time.time()
+    while time.time() - t_soak < 0.6:  # let the sampler see the GPU under this load
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(K):
+        step(evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    ms = t0.elapsed_time(t1) / K
+    stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j, s in enumerate(STAGES)}
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public call with host buffers: H2D of the step's inputs
+    # from pinned memory, the layer, D2H of the result, all inside the timed region
+    hx = li.x.cpu().pin_memory()
+    hids = li.topk_ids.cpu().pin_memory()
+    hw = li.topk_weights.cpu().pin_memory()
+    hout = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
+    dx, dids, dw = torch.empty_like(li.x), torch.empty_like(li.topk_ids), torch.empty_like(
+        li.topk_weights)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        layer(dx, dids, dw, out=out, sched=sched, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
+    d2h = hout.numel() * 2
+
+    rc, flags = qmoe.qmoe_read_error(ws)
+    if rc != 0:
+        raise RuntimeError(f"device error word after the timed region: rc={rc} flags={flags}")
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_kind = load_peaks()
+    alg = algorithmic_bytes(cfg, li.topk_ids.cpu())
+    decode = (sched == qmoe.QMOE_SCHED_DECODE or
+              (sched == qmoe.QMOE_SCHED_AUTO and M * top_k <= 4 * E))
+    sched_name = "decode" if decode else "prefill"
+    if decode:
+        dom = "fc1"
+        ach = alg["fc1"] / (stage_ms["fc1"] * 1e-3) / 1e9
+        roof = {"kernel": f"moe_gemm_kernel<FC1,{sched_name}>", "bound": "hbm",
+                "achieved": ach, "peak": hbm_gbs, "unit": "GB/s", "frac": ach / hbm_gbs,
+                "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
+                "algorithmic_bytes_per_launch": alg["fc1"],
+                "traffic": measured_traffic("fc1", cfg.name)}
+    else:
+        dom = "fc1"
+        fl = 2.0 * alg["pairs"] * 2 * H * I
+        ach = fl / (stage_ms["fc1"] * 1e-3) / 1e12
+        roof = {"kernel": f"moe_gemm_kernel<FC1,{sched_name}>", "bound": "tensor",
+                "achieved": ach, "peak": bf16_tf, "unit": "TFLOP/s", "frac": ach / bf16_tf,
+                "peak_kind": f"{peak_kind} (bf16_tflops, burst)",
+                "algorithmic_flops_per_launch": fl,
+                "traffic": measured_traffic("fc1", cfg.name)}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n_tok = max(1, min(M, oracle.max_threads()))
+        v, dt, threads, n = run_cpu_oracle(li, n_tok)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} of {M} tokens (all their top_k slots), {dt:.1f} s"}
+
+    value = world * M / (ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "M": M, "H": H, "I": I, "E": E, "top_k": top_k,
+                   "sched": sched_name, "global_batch": world * M,
+                   "l2": f"inputs larger than L2: {alg['weights'] / 1e9:.2f} GB of touched "
+                         f"expert weights streamed per step",
+                   "parallelism": f"replicas{world}"},
+        "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * K,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "clocks": sampler.summary(),
+        "stages_ms": stage_ms,
+        "weight_gbs": alg["weights"] / (ms * 1e-3) / 1e9,
+        "hbm_frac_layer": alg["weights"] / (ms * 1e-3) / 1e9 / hbm_gbs,
+        "tflops": alg["flops"] / (ms * 1e-3) / 1e12,
+        "touched_experts": alg["touched_experts"],
+        "repack_ms": repack_ms,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    return ours_arm(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * qmoe — NVFP4 W4A16 mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * The layer (megamoe_rm.cu page: header comment, route_prep, fc1_rm, fc2_rm,
+ * combine; tilelang_kernels.py page: grouped_gemm_fp4):
+ *   pairs i = m * top_k + k of M tokens and top_k slots are grouped by expert;
+ *   for each pair with expert e:
+ *     g   = gs13[e] * x[m] . Wq13[e]^T        (Wq13 [2I][H]: rows 0..I-1 up, I..2I-1 gate)
+ *     h   = bf16( SiLU(g[I:2I]) * g[0:I] )
+ *     y   = gs2[e] * h . Wq2[e]^T             (Wq2 [H][I])
+ *   out[m] = bf16( sum over k ascending of topk_weights[m][k] * y_(m,k) )
+ * Wq = E2M1 code * E4M3 block scale (one scale per 16 K-elements of a row); two
+ * codes per byte along K, the even K element in the low nibble.  x is bf16.
+ *
+ * Conventions for every call:
+ *  - Pointers named *_dev are device pointers owned by the caller; the library
+ *    never allocates, frees or keeps them.  `stream` is a cudaStream_t (may be
+ *    NULL for the legacy default stream); all work is enqueued on it and no call
+ *    synchronises the host, except qmoe_read_error.
+ *  - Every call returns QMOE_OK (0) or a negative QMOE_ERR_* code and never
+ *    throws or aborts.  Argument checks run before anything is enqueued.
+ *  - Shapes: H % 128 == 0, I % 128 == 0, 1 <= E <= 2048, 1 <= top_k <= 64,
+ *    M >= 0 (M == 0 is a no-op), M * top_k < 2^31, H, I <= 65536.
+ *  - The device must be sm_103 (GB300) or another sm_10x part running sm_103a
+ *    code; otherwise QMOE_ERR_ARCH.
+ */
+#ifndef QMOE_H_
+#define QMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMOE_OK 0
+#define QMOE_ERR_ARG (-1)       /* null pointer or argument out of range */
+#define QMOE_ERR_SHAPE (-2)     /* dimensions violate the shape rules above */
+#define QMOE_ERR_CUDA (-3)      /* a CUDA runtime call or launch failed */
+#define QMOE_ERR_TIMEOUT (-4)   /* a bounded device-side wait expired (qmoe_read_error) */
+#define QMOE_ERR_ARCH (-5)      /* the current device cannot run sm_103a code */
+#define QMOE_ERR_WORKSPACE (-6) /* workspace smaller than the size query returned */
+#define QMOE_ERR_BAD_ID (-7)    /* an expert id >= E was seen (qmoe_read_error) */
+
+/* Device error-word bits (qmoe_read_error). */
+#define QMOE_FLAG_BAD_ID 1u
+#define QMOE_FLAG_TIMEOUT 2u
+
+/* Tile schedules for moe_nvfp4_forward. */
+#define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
+#define QMOE_SCHED_DECODE 1  /* tiles of <= 32 pairs: weight streaming, HBM bound */
+#define QMOE_SCHED_PREFILL 2 /* tiles of <= 256 pairs: tensor bound */
+
+/* Weight roles for moe_nvfp4_repack. */
+#define QMOE_W13 1 /* w13 [E][2I][H/2]: up and gate rows, interleaved for the SwiGLU epilogue */
+#define QMOE_W2 2  /* w2  [E][H][I/2] */
+
+/* Pair-tile height used by each schedule (the moe_route tile_n it runs with). */
+int qmoe_sched_tile_n(int sched, int M, int top_k, int E);
+
+/* Upper bound on the number of tiles moe_route can emit: ceil(M*top_k/tile_n) + E. */
+int qmoe_max_tiles(int M, int top_k, int E, int tile_n);
+
+/*
+ * moe_route — group the M*top_k (token, expert) pairs by expert.
+ * Defined by route_prep on the megamoe_rm.cu page (a pair's slot is its rank among
+ * earlier pairs with the same expert; expert -1 is skipped) and by the per-expert
+ * row offsets of cutlass discussion 2855 ("total tokens including expert").
+ *   topk_ids_dev     int32 [M][top_k], row-major; pair i = m * top_k + k.  Ids < 0
+ *                    are skipped; ids >= E are skipped and set QMOE_FLAG_BAD_ID in
+ *                    the error word (first 4 bytes of `workspace_dev`).
+ *   offsets_dev      int32 [E+1]: offsets[e] = valid pairs with expert < e.
+ *   sorted_pair_dev  int32 [M*top_k]: pairs in (expert, pair index) order; entries
+ *                    at positions >= offsets[E] are -1.
+ *   pair_pos_dev     int32 [M*top_k]: inverse of sorted_pair, -1 for skipped pairs.
+ *   tiles_dev        int32 [qmoe_max_tiles(...)][3]: (expert, start position, rows),
+ *                    rows <= tile_n, experts ascending, positions ascending; only
+ *                    the first *n_tiles entries are written.
+ *   n_tiles_dev      int32 [1].
+ *   workspace_dev    >= qmoe_route_workspace_size(...) bytes; its first 4 bytes are
+ *                    the error word, which this call clears first.
+ * The result is bit-exact and deterministic.
+ */
+size_t qmoe_route_workspace_size(int M, int top_k, int E, int tile_n);
+int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
+              int32_t* offsets_dev, int32_t* sorted_pair_dev, int32_t* pair_pos_dev,
+              int32_t* tiles_dev, int32_t* n_tiles_dev, void* workspace_dev, size_t ws_bytes,
+              void* stream);
+
+/*
+ * moe_nvfp4_repack — one-time reordering of plain NVFP4 weights into the layout
+ * the grouped GEMM streams (a kernel-chosen layout; bytes are only permuted, the
+ * sizes equal the inputs').  The principle follows cutlass issue 2087: store the
+ * scales in the order the loader consumes them, so tile loads are contiguous.
+ *   w_fp4_dev    uint8 [E][N][K/2]  plain codes (low nibble = even k)
+ *   w_scale_dev  uint8 [E][N][K/16] plain E4M3 block scales
+ *   which        QMOE_W13 (N = 2I, K = H) or QMOE_W2 (N = H, K = I)
+ *   out_fp4_dev  uint8, qmoe_repacked_fp4_size(E, N, K) bytes
+ *   out_scale_dev uint8, qmoe_repacked_scale_size(E, N, K) bytes
+ * N % 128 == 0 and K % 128 == 0 are required (QMOE_ERR_SHAPE otherwise).
+ */
+size_t qmoe_repacked_fp4_size(int E, int N, int K);
+size_t qmoe_repacked_scale_size(int E, int N, int K);
+int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N, int K,
+                     int which, uint8_t* out_fp4_dev, uint8_t* out_scale_dev, void* stream);
+
+/*
+ * moe_nvfp4_forward — the whole layer: route, gather, grouped FC1 + SwiGLU, grouped
+ * FC2, weighted top_k combine.  Follows megamoe_rm_forward on the megamoe_rm.cu
+ * page (scratch passed in by the caller, work on the caller's stream, shape
+ * checks up front).
+ *   x_dev           bf16 [M][H]
+ *   w13_fp4_dev, w13_scale_dev   repacked w13 (moe_nvfp4_repack with QMOE_W13)
+ *   w13_gscale_dev  fp32 [E], multiplies the FC1 accumulator
+ *   w2_fp4_dev, w2_scale_dev     repacked w2 (moe_nvfp4_repack with QMOE_W2)
+ *   w2_gscale_dev   fp32 [E], multiplies the FC2 accumulator
+ *   topk_ids_dev    int32 [M][top_k]  (ids < 0 skipped, ids >= E flagged and skipped)
+ *   topk_weights_dev fp32 [M][top_k], used as given
+ *   out_dev         bf16 [M][H]
+ *   sched           QMOE_SCHED_*
+ *   workspace_dev   >= qmoe_forward_workspace_size(M, H, I, E, top_k, sched) bytes,
+ *                   256-byte aligned; holds the error word, routing tables, the
+ *                   gathered activations, h and the per-pair partial outputs.
+ * Deterministic: two calls on the same inputs give bitwise equal outputs.  Calls
+ * sharing one workspace must not overlap on the GPU.
+ */
+size_t qmoe_forward_workspace_size(int M, int H, int I, int E, int top_k, int sched);
+int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8_t* w13_scale_dev,
+                      const float* w13_gscale_dev, const uint8_t* w2_fp4_dev,
+                      const uint8_t* w2_scale_dev, const float* w2_gscale_dev,
+                      const int32_t* topk_ids_dev, const float* topk_weights_dev, void* out_dev,
+                      int M, int H, int I, int E, int top_k, int sched, void* workspace_dev,
+                      size_t ws_bytes, void* stream);
+
+/*
+ * moe_nvfp4_forward_events — moe_nvfp4_forward that also records six caller-owned
+ * cudaEvent_t at its stage boundaries on `stream`, so that each kernel can be timed
+ * on the stream it runs on: events[0] before route, [1] after route, [2] after the
+ * activation gather, [3] after FC1, [4] after FC2, [5] after combine.  Same
+ * arguments, results and errors as moe_nvfp4_forward; QMOE_ERR_ARG if `events` or
+ * any of its six entries is NULL.  (A measurement hook; no counterpart on the pages.)
+ */
+int moe_nvfp4_forward_events(const void* x_dev, const uint8_t* w13_fp4_dev,
+                             const uint8_t* w13_scale_dev, const float* w13_gscale_dev,
+                             const uint8_t* w2_fp4_dev, const uint8_t* w2_scale_dev,
+                             const float* w2_gscale_dev, const int32_t* topk_ids_dev,
+                             const float* topk_weights_dev, void* out_dev, int M, int H, int I,
+                             int E, int top_k, int sched, void* workspace_dev, size_t ws_bytes,
+                             void* stream, void* const* events);
+
+/*
+ * qmoe_read_error — copy the device error word (first 4 bytes of a route or forward
+ * workspace) to the host after the stream's work so far; synchronises `stream`.
+ * *flags_out gets the QMOE_FLAG_* bits.  Returns QMOE_ERR_TIMEOUT if the timeout
+ * bit is set, else QMOE_ERR_BAD_ID if the bad-id bit is set, else QMOE_OK.
+ */
+int qmoe_read_error(const void* workspace_dev, void* stream, uint32_t* flags_out);
+
+/*
+ * Diagnostics used by the tests (no counterpart on the pages).
+ * qmoe_selftest_dequant: for every E2M1 code c (0..15) and E4M3 scale byte s
+ *   (0..255) writes the kernel's dequantized bf16 of code*scale to
+ *   out_dev[c * 256 + s] (uint16 bf16 bits, 4096 entries).  The product is exact.
+ * qmoe_selftest_timeout: runs the bounded mbarrier wait of the GEMM kernels on a
+ *   barrier nothing arrives at, with a limit of `limit_ns` nanoseconds, and records
+ *   the expiry in the error word at workspace_dev (>= 256 bytes).  Returns
+ *   QMOE_ERR_TIMEOUT when the wait expired as it must, QMOE_OK otherwise.
+ */
+int qmoe_selftest_dequant(uint16_t* out_dev, void* stream);
+int qmoe_selftest_timeout(void* workspace_dev, long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_H_ */

@@ -131,26 +131,42 @@ def _routing(cfg: LayerConfig, g: torch.Generator, device):
     return ids.to(torch.int32).contiguous(), wts.float().contiguous()
 
 
+def expert_seed(seed: int, e: int) -> int:
+    """Seed of expert e's weight draws: each expert has its own stream, so any subset
+    of experts can be generated alone with the same bytes."""
+    return (seed + 1) * 1_000_003 + 7919 * (e + 1)
+
+
 def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None,
-                weight_std: float = 0.02) -> LayerInputs:
-    """Draw one layer's inputs with the config's recipe on `device`."""
+                weight_std: float = 0.02, token_seed: Optional[int] = None,
+                experts=None) -> LayerInputs:
+    """Draw one layer's inputs with the config's recipe on `device`.
+
+    `token_seed` (default: the config seed) seeds x and the routing; weights are
+    drawn per expert from expert_seed(seed, e).  With `experts` given, only those
+    experts' weights are drawn and the others are left as zero bytes."""
     device = torch.device(device)
+    seed = cfg.seed if seed is None else seed
     g = torch.Generator(device=device)
-    g.manual_seed(cfg.seed if seed is None else seed)
+    g.manual_seed(seed if token_seed is None else token_seed)
     M, H, I, E = cfg.M, cfg.H, cfg.I, cfg.E
     x = torch.randn(M, H, generator=g, device=device).to(torch.bfloat16)
     ids, wts = _routing(cfg, g, device)
-    w13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-    s13 = torch.empty(E, 2 * I, H // 16, dtype=torch.uint8, device=device)
-    w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
-    s2 = torch.empty(E, H, I // 16, dtype=torch.uint8, device=device)
-    gs13 = torch.empty(E, dtype=torch.float32, device=device)
-    gs2 = torch.empty(E, dtype=torch.float32, device=device)
-    for e in range(E):
-        wa = torch.randn(2 * I, H, generator=g, device=device) * weight_std
+    w13 = torch.zeros(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
+    s13 = torch.zeros(E, 2 * I, H // 16, dtype=torch.uint8, device=device)
+    w2 = torch.zeros(E, H, I // 2, dtype=torch.uint8, device=device)
+    s2 = torch.zeros(E, H, I // 16, dtype=torch.uint8, device=device)
+    gs13 = torch.ones(E, dtype=torch.float32, device=device)
+    gs2 = torch.ones(E, dtype=torch.float32, device=device)
+    for e in (range(E) if experts is None else sorted(set(int(v) for v in experts))):
+        ge = torch.Generator(device=device)
+        ge.manual_seed(expert_seed(seed, e))
+        wa = torch.randn(2 * I, H, generator=ge, device=device) * weight_std
         w13[e], s13[e], gs13[e] = quantize_nvfp4(wa)
-        wb = torch.randn(H, I, generator=g, device=device) * weight_std
+        del wa
+        wb = torch.randn(H, I, generator=ge, device=device) * weight_std
         w2[e], s2[e], gs2[e] = quantize_nvfp4(wb)
+        del wb
     return LayerInputs(cfg, x.contiguous(), ids, wts, w13, s13, gs13, w2, s2, gs2)
 
 

@@ -1,0 +1,337 @@
+// C-ABI boundary of libqmoe: argument checks, workspace layout, tensor maps and
+// the launch sequence of the layer (megamoe_rm.cu page, megamoe_rm_forward: shape
+// checks, scratch carved from caller memory, everything on the caller's stream).
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace qmoe {
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_num_sms[kMaxDevices];
+int g_arch_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 unsupported
+
+int device_info(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMOE_ERR_CUDA;
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QMOE_ERR_CUDA;
+    g_num_sms[dev] = sms;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_arch_ok[dev] < 0) return QMOE_ERR_ARCH;
+  *num_sms = g_num_sms[dev];
+  return QMOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Row-major bf16 [rows][cols] operand, boxes of 64 columns x 16 rows, 128-byte swizzle.
+int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols) {
+  auto fn = encode_fn();
+  if (!fn) return QMOE_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? QMOE_OK : QMOE_ERR_CUDA;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct ForwardLayout {
+  size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, xs, h, ypart, total;
+  int rows;  // rows of xs / h (>= 16, multiple of 16)
+  int tile_n, max_tiles;
+};
+
+int check_shape(int M, int H, int I, int E, int top_k) {
+  if (M < 0 || E < 1 || E > 2048 || top_k < 1 || top_k > 64) return QMOE_ERR_SHAPE;
+  if (H < 128 || I < 128 || H % 128 || I % 128 || H > 65536 || I > 65536) return QMOE_ERR_SHAPE;
+  if ((long long)M * top_k >= (1LL << 31) / 16) return QMOE_ERR_SHAPE;
+  return QMOE_OK;
+}
+
+int resolve_sched(int sched, int M, int top_k, int E) {
+  if (sched == QMOE_SCHED_DECODE || sched == QMOE_SCHED_PREFILL) return sched;
+  return (long long)M * top_k <= 4LL * E ? QMOE_SCHED_DECODE : QMOE_SCHED_PREFILL;
+}
+
+ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {
+  ForwardLayout L;
+  const long long P = (long long)M * top_k;
+  L.tile_n = gemm_tile_n(resolve_sched(sched, M, top_k, E));
+  L.max_tiles = (int)((P + L.tile_n - 1) / L.tile_n) + E;
+  L.rows = (int)align_up((size_t)(P > 0 ? P : 1), 16);
+  size_t off = kWsHeaderBytes;
+  L.offsets = off;
+  off = align_up(off + 4 * (size_t)(E + 1), 256);
+  L.sorted_pair = off;
+  off = align_up(off + 4 * (size_t)P, 256);
+  L.pair_pos = off;
+  off = align_up(off + 4 * (size_t)P, 256);
+  L.tiles = off;
+  off = align_up(off + 12 * (size_t)L.max_tiles, 256);
+  L.n_tiles = off;
+  off = align_up(off + 4, 1024);
+  L.xs = off;
+  off = align_up(off + 2 * (size_t)L.rows * H, 1024);
+  L.h = off;
+  off = align_up(off + 2 * (size_t)L.rows * I, 1024);
+  L.ypart = off;
+  off = align_up(off + 4 * (size_t)P * H, 256);
+  L.total = off;
+  return L;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace qmoe
+
+using namespace qmoe;
+
+extern "C" {
+
+int qmoe_sched_tile_n(int sched, int M, int top_k, int E) {
+  return gemm_tile_n(resolve_sched(sched, M, top_k, E));
+}
+
+int qmoe_max_tiles(int M, int top_k, int E, int tile_n) {
+  if (M < 0 || top_k < 1 || E < 1 || tile_n < 1) return QMOE_ERR_ARG;
+  const long long P = (long long)M * top_k;
+  return (int)((P + tile_n - 1) / tile_n) + E;
+}
+
+size_t qmoe_route_workspace_size(int M, int top_k, int E, int tile_n) {
+  (void)M;
+  (void)top_k;
+  (void)E;
+  (void)tile_n;
+  return kWsHeaderBytes;
+}
+
+int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
+              int32_t* offsets_dev, int32_t* sorted_pair_dev, int32_t* pair_pos_dev,
+              int32_t* tiles_dev, int32_t* n_tiles_dev, void* workspace_dev, size_t ws_bytes,
+              void* stream) {
+  if (M < 0 || top_k < 1 || top_k > 64 || E < 1 || E > 2048 || tile_n < 1 || tile_n > 4096)
+    return QMOE_ERR_SHAPE;
+  if ((long long)M * top_k >= (1LL << 31) / 16) return QMOE_ERR_SHAPE;
+  if (!offsets_dev || !n_tiles_dev || !workspace_dev || !tiles_dev) return QMOE_ERR_ARG;
+  if (M > 0 && (!topk_ids_dev || !sorted_pair_dev || !pair_pos_dev)) return QMOE_ERR_ARG;
+  if (ws_bytes < qmoe_route_workspace_size(M, top_k, E, tile_n)) return QMOE_ERR_WORKSPACE;
+  int sms = 0;
+  int rc = device_info(&sms);
+  if (rc != QMOE_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace_dev, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
+  return cuda_rc(launch_route(topk_ids_dev, M * top_k, E, tile_n, offsets_dev, sorted_pair_dev,
+                              pair_pos_dev, tiles_dev, n_tiles_dev,
+                              reinterpret_cast<unsigned int*>(workspace_dev), s));
+}
+
+size_t qmoe_repacked_fp4_size(int E, int N, int K) {
+  if (E < 1 || N < 1 || K < 1) return 0;
+  return (size_t)E * N * (K / 2);
+}
+
+size_t qmoe_repacked_scale_size(int E, int N, int K) {
+  if (E < 1 || N < 1 || K < 1) return 0;
+  return (size_t)E * N * (K / 16);
+}
+
+int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N, int K,
+                     int which, uint8_t* out_fp4_dev, uint8_t* out_scale_dev, void* stream) {
+  if (which != QMOE_W13 && which != QMOE_W2) return QMOE_ERR_ARG;
+  if (E < 1 || E > 2048 || N < 128 || K < 128 || N % 128 || K % 128 || N > 131072 || K > 65536)
+    return QMOE_ERR_SHAPE;
+  if (!w_fp4_dev || !w_scale_dev || !out_fp4_dev || !out_scale_dev) return QMOE_ERR_ARG;
+  if (((uintptr_t)w_fp4_dev | (uintptr_t)w_scale_dev | (uintptr_t)out_fp4_dev |
+       (uintptr_t)out_scale_dev) & 15)
+    return QMOE_ERR_ARG;
+  int sms = 0;
+  int rc = device_info(&sms);
+  if (rc != QMOE_OK) return rc;
+  return cuda_rc(launch_repack(w_fp4_dev, w_scale_dev, E, N, K, which == QMOE_W13, out_fp4_dev,
+                               out_scale_dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qmoe_forward_workspace_size(int M, int H, int I, int E, int top_k, int sched) {
+  if (check_shape(M, H, I, E, top_k) != QMOE_OK) return 0;
+  return forward_layout(M, H, I, E, top_k, sched).total;
+}
+
+static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8_t* w13_scale_dev,
+                        const float* w13_gscale_dev, const uint8_t* w2_fp4_dev,
+                        const uint8_t* w2_scale_dev, const float* w2_gscale_dev,
+                        const int32_t* topk_ids_dev, const float* topk_weights_dev, void* out_dev,
+                        int M, int H, int I, int E, int top_k, int sched, void* workspace_dev,
+                        size_t ws_bytes, void* stream, void* const* events) {
+  int rc = check_shape(M, H, I, E, top_k);
+  if (rc != QMOE_OK) return rc;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL) return QMOE_ERR_ARG;
+  if (M == 0) return QMOE_OK;
+  if (!x_dev || !w13_fp4_dev || !w13_scale_dev || !w13_gscale_dev || !w2_fp4_dev ||
+      !w2_scale_dev || !w2_gscale_dev || !topk_ids_dev || !topk_weights_dev || !out_dev ||
+      !workspace_dev)
+    return QMOE_ERR_ARG;
+  if (((uintptr_t)x_dev | (uintptr_t)out_dev | (uintptr_t)w13_fp4_dev | (uintptr_t)w13_scale_dev |
+       (uintptr_t)w2_fp4_dev | (uintptr_t)w2_scale_dev) & 15)
+    return QMOE_ERR_ARG;
+  if ((uintptr_t)workspace_dev & 255) return QMOE_ERR_ARG;
+  const ForwardLayout L = forward_layout(M, H, I, E, top_k, sched);
+  if (ws_bytes < L.total) return QMOE_ERR_WORKSPACE;
+  int sms = 0;
+  rc = device_info(&sms);
+  if (rc != QMOE_OK) return rc;
+  const int rsched = resolve_sched(sched, M, top_k, E);
+  const int P = M * top_k;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace_dev);
+  unsigned int* err = reinterpret_cast<unsigned int*>(ws);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* sorted_pair = reinterpret_cast<int32_t*>(ws + L.sorted_pair);
+  int32_t* pair_pos = reinterpret_cast<int32_t*>(ws + L.pair_pos);
+  int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.tiles);
+  int32_t* n_tiles = reinterpret_cast<int32_t*>(ws + L.n_tiles);
+  void* xs = ws + L.xs;
+  void* h = ws + L.h;
+  float* ypart = reinterpret_cast<float*>(ws + L.ypart);
+
+  CUtensorMap map_x, map_h;
+  if (make_tmap_rows(&map_x, xs, L.rows, H) != QMOE_OK) return QMOE_ERR_CUDA;
+  if (make_tmap_rows(&map_h, h, L.rows, I) != QMOE_OK) return QMOE_ERR_CUDA;
+
+  auto mark = [&](int i) -> bool {
+    return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+  };
+  if (cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
+  if (!mark(0)) return QMOE_ERR_CUDA;
+  cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
+                               n_tiles, err, s);
+  if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
+  e = launch_gather(x_dev, sorted_pair, offsets + E, top_k, H, P, xs, sms, s);
+  if (e != cudaSuccess || !mark(2)) return QMOE_ERR_CUDA;
+
+  GemmParams p1;
+  memset(&p1, 0, sizeof(p1));
+  p1.wcodes = w13_fp4_dev;
+  p1.wscales = w13_scale_dev;
+  p1.gscale = w13_gscale_dev;
+  p1.tiles = tiles;
+  p1.n_tiles = n_tiles;
+  p1.K = H;
+  p1.nrb = 2 * I / 128;
+  p1.h = h;
+  p1.I = I;
+  p1.err = err;
+  e = launch_gemm(GemmKind::kFc1, rsched, map_x, p1, sms, s);
+  if (e != cudaSuccess || !mark(3)) return QMOE_ERR_CUDA;
+
+  GemmParams p2;
+  memset(&p2, 0, sizeof(p2));
+  p2.wcodes = w2_fp4_dev;
+  p2.wscales = w2_scale_dev;
+  p2.gscale = w2_gscale_dev;
+  p2.tiles = tiles;
+  p2.n_tiles = n_tiles;
+  p2.K = I;
+  p2.nrb = H / 128;
+  p2.ypart = ypart;
+  p2.sorted_pair = sorted_pair;
+  p2.topk_w = topk_weights_dev;
+  p2.H = H;
+  p2.err = err;
+  e = launch_gemm(GemmKind::kFc2, rsched, map_h, p2, sms, s);
+  if (e != cudaSuccess || !mark(4)) return QMOE_ERR_CUDA;
+
+  e = launch_combine(ypart, topk_ids_dev, M, top_k, E, H, out_dev, sms, s);
+  if (e != cudaSuccess || !mark(5)) return QMOE_ERR_CUDA;
+  return QMOE_OK;
+}
+
+int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8_t* w13_scale_dev,
+                      const float* w13_gscale_dev, const uint8_t* w2_fp4_dev,
+                      const uint8_t* w2_scale_dev, const float* w2_gscale_dev,
+                      const int32_t* topk_ids_dev, const float* topk_weights_dev, void* out_dev,
+                      int M, int H, int I, int E, int top_k, int sched, void* workspace_dev,
+                      size_t ws_bytes, void* stream) {
+  return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
+                      w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
+                      sched, workspace_dev, ws_bytes, stream, nullptr);
+}
+
+int moe_nvfp4_forward_events(const void* x_dev, const uint8_t* w13_fp4_dev,
+                             const uint8_t* w13_scale_dev, const float* w13_gscale_dev,
+                             const uint8_t* w2_fp4_dev, const uint8_t* w2_scale_dev,
+                             const float* w2_gscale_dev, const int32_t* topk_ids_dev,
+                             const float* topk_weights_dev, void* out_dev, int M, int H, int I,
+                             int E, int top_k, int sched, void* workspace_dev, size_t ws_bytes,
+                             void* stream, void* const* events) {
+  if (!events) return QMOE_ERR_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!events[i]) return QMOE_ERR_ARG;
+  return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
+                      w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
+                      sched, workspace_dev, ws_bytes, stream, events);
+}
+
+int qmoe_read_error(const void* workspace_dev, void* stream, uint32_t* flags_out) {
+  if (!workspace_dev || !flags_out) return QMOE_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t flags = 0;
+  if (cudaMemcpyAsync(&flags, workspace_dev, sizeof(flags), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return QMOE_ERR_CUDA;
+  *flags_out = flags;
+  if (flags & QMOE_FLAG_TIMEOUT) return QMOE_ERR_TIMEOUT;
+  if (flags & QMOE_FLAG_BAD_ID) return QMOE_ERR_BAD_ID;
+  return QMOE_OK;
+}
+
+int qmoe_selftest_dequant(uint16_t* out_dev, void* stream) {
+  if (!out_dev) return QMOE_ERR_ARG;
+  int sms = 0;
+  int rc = device_info(&sms);
+  if (rc != QMOE_OK) return rc;
+  return cuda_rc(launch_selftest_dequant(out_dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qmoe_selftest_timeout(void* workspace_dev, long long limit_ns, void* stream) {
+  if (!workspace_dev || limit_ns < 1000 || limit_ns > 1000000000LL) return QMOE_ERR_ARG;
+  int sms = 0;
+  int rc = device_info(&sms);
+  if (rc != QMOE_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace_dev, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
+  if (launch_selftest_timeout(reinterpret_cast<unsigned int*>(workspace_dev), limit_ns, s) !=
+      cudaSuccess)
+    return QMOE_ERR_CUDA;
+  uint32_t flags = 0;
+  return qmoe_read_error(workspace_dev, stream, &flags);
+}
+
+}  // extern "C"

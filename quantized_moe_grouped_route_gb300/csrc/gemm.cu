@@ -1,0 +1,312 @@
+// Persistent grouped GEMM for FC1 (+ SwiGLU) and FC2 (+ global scale and routing
+// weight) of the NVFP4 W4A16 MoE layer, on tcgen05 tensor cores.
+//
+// What it computes (megamoe_rm.cu page, fc1_rm / fc2_rm; spec layer):
+//   FC1 tile (expert e, 128 weight rows rb, pair tile t):
+//     g = gs13[e] * Wq13[e][rows] . xs[t]^T, then h = bf16(SiLU(gate) * up)
+//   FC2 tile: y = gs2[e] * Wq2[e][rows] . h[t]^T, ypart[pair][j] = topk_w[pair] * y
+// Each unit is one 128-row block of one expert's weights against one tile of that
+// expert's pairs (<= NMAX pairs) over the whole K: the weights are the MMA's M side
+// ("swap AB": weight rows on M = 128, pairs on N = 16..NMAX), so small per-expert
+// batches still fill the instruction, and every output element is produced by one
+// CTA in a fixed order (deterministic, no split reduction).
+//
+// Data path per 128-wide K step (one pipeline stage):
+//   TMA warp      : bulk copy of the step's packed codes (8 KB) and scales (1 KB),
+//                   tiled TMA of the pair rows (bf16, 128-byte swizzle) -> smem ring
+//   dequant warps : codes -> bf16 in registers (bit placement + one bf16x2 multiply
+//                   by the block scale) -> tcgen05.st into TMEM (the MMA's A operand)
+//   MMA thread    : 8 x tcgen05.mma kind::f16, A from TMEM, B from smem, fp32
+//                   accumulator in TMEM; commits release the stage
+//   epilogue warps: tcgen05.ld of the accumulator, scale, SwiGLU or routing weight,
+//                   global stores
+// The dequantized weights never touch shared memory, which leaves the smem
+// bandwidth to TMA and the MMA's B reads.
+//
+// Every wait is bounded (qmoe::mbar_wait): on expiry the CTA raises the timeout bit
+// in the error word, the roles leave their loops, in-flight copies and MMAs are
+// drained with bounded waits, and TMEM is released before the CTA exits.
+#include "common.cuh"
+#include "dequant.cuh"
+#include "launch.h"
+
+namespace qmoe {
+namespace {
+
+constexpr int kThreads = 448;       // 14 warps
+constexpr int kBK = 128;            // K per stage
+constexpr int kCodeBytes = 8192;    // 128 rows x 128 K / 2
+constexpr int kScaleBytes = 1024;   // 128 rows x 8 blocks
+constexpr int kTmemCols = 512;
+constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale table
+
+template <int NMAX, int STAGES, int ACCB>
+struct Cfg {
+  static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
+  static constexpr int kBBytes = 2 * kBSlab;
+  static constexpr int kStageBytes = kBBytes + kCodeBytes + kScaleBytes;
+  static constexpr int kAccCol0 = STAGES * 64;  // TMEM: [A slots: 64 cols each][accumulators]
+  static constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + kCtrlBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(STAGES * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
+  static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((long long)(globaltimer_ns() - t0) > 50000000LL) return false;  // 50 ms
+  }
+  return true;
+}
+
+template <int NMAX, int STAGES, int ACCB, bool FC1>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  using C = Cfg<NMAX, STAGES, ACCB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* ctrl = smem + STAGES * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // TMA bytes landed
+  uint64_t* deq = full + STAGES;                        // A slot written (4 warps)
+  uint64_t* empty = deq + STAGES;                       // MMA finished reading the stage
+  uint64_t* accf = empty + STAGES;                      // accumulator ready
+  uint64_t* acce = accf + ACCB;                         // accumulator drained (4 warps)
+  uint64_t* drain = acce + ACCB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* scale_lut = reinterpret_cast<uint32_t*>(ctrl + 1024);  // [256]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&deq[s]), 4);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < ACCB; ++a) {
+      mbar_init(smem_u32(&accf[a]), 1);
+      mbar_init(smem_u32(&acce[a]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int b = threadIdx.x; b < 256; b += kThreads) scale_lut[b] = e4m3_scale_bf16x2(b);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_b);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int nks = p.K / kBK;
+  const int n_units = (*p.n_tiles) * p.nrb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int t = u / p.nrb, rb = u - t * p.nrb;
+        const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
+        const int nb16 = (rows + 15) >> 4;
+        const uint32_t tx = kCodeBytes + kScaleBytes + 2u * (uint32_t)nb16 * 2048u;
+        const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nks;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * C::kStageBytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, tx);
+          bulk_g2s(smem_u32(st + C::kBBytes), p.wcodes + (blk + ks) * kCodeBytes, kCodeBytes, fb,
+                   pol_w);
+          bulk_g2s(smem_u32(st + C::kBBytes + kCodeBytes), p.wscales + (blk + ks) * kScaleBytes,
+                   kScaleBytes, fb, pol_w);
+#pragma unroll
+          for (int sl = 0; sl < 2; ++sl)
+            for (int g = 0; g < nb16; ++g)
+              tma_load_2d(smem_u32(st + sl * C::kBSlab + g * 2048), &tmap_b, ks * kBK + sl * 64,
+                          start + g * 16, fb, pol_b);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA can exit
+        const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, local = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
+        const int t = u / p.nrb;
+        const int rows = p.tiles[3 * t + 2];
+        const uint32_t idesc = idesc_bf16_f32(128, ((rows + 15) >> 4) << 4);
+        const int ab = local % ACCB;
+        const uint32_t aph = (local / ACCB) & 1;
+        if (!mbar_wait(smem_u32(&acce[ab]), aph ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err) ||
+              !mbar_wait(smem_u32(&deq[s]), ph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(smem + s * C::kStageBytes);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t baddr = b0 + (j >> 2) * C::kBSlab + (j & 3) * 32;
+            mma_bf16_ts(d_tmem, tmem + s * 64 + j * 8, sdesc_sw128(baddr), idesc,
+                        (ks | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[s]));
+        }
+        if (ok) tc_commit(smem_u32(&accf[ab]));
+      }
+      // no MMA may still be running when TMEM is released
+      tc_commit(smem_u32(drain));
+      drain_wait(smem_u32(drain), 0);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ dequant warps
+    const int grp = (warp - 6) >> 2;  // which stages: it % 2 == grp
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;    // weight row of the 128-row block
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        if ((int)(it & 1) != grp) continue;
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* st = smem + s * C::kStageBytes;
+        const uint4* codes = reinterpret_cast<const uint4*>(st + C::kBBytes);
+        const uint2 sc = *reinterpret_cast<const uint2*>(st + C::kBBytes + kCodeBytes + row * 8);
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + s * 64;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 cw = codes[kk * 128 + row];
+          const uint32_t sb = (kk < 2) ? sc.x : sc.y;
+          const int sh = 16 * (kk & 1);
+          const uint32_t s0 = scale_lut[(sb >> sh) & 0xFF];
+          const uint32_t s1 = scale_lut[(sb >> (sh + 8)) & 0xFF];
+          uint32_t o[16];
+          dequant8(cw.x, s0, o + 0);
+          dequant8(cw.y, s0, o + 4);
+          dequant8(cw.z, s1, o + 8);
+          dequant8(cw.w, s1, o + 12);
+          tmem_st_x16(ta + kk * 16, o);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&deq[s]));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..5
+    const int q = warp & 3;
+    uint32_t local = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
+      const int t = u / p.nrb, rb = u - t * p.nrb;
+      const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
+      const int ab = local % ACCB;
+      const uint32_t aph = (local / ACCB) & 1;
+      if (!mbar_wait(smem_u32(&accf[ab]), aph, abort_flag, p.err)) break;
+      tc_fence_after();
+      const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMAX;
+      for (int c0 = 0; c0 < rows; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tbase + c0, v);
+        tmem_wait_ld();
+        if constexpr (FC1) {
+          // lanes 0..15: up rows, lanes 16..31: gate rows of the same 16 indices
+          const int i = rb * 64 + q * 16 + (lane & 15);
+          __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float mine = __uint_as_float(v[c]) * gsc;
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            if (lane < 16 && c0 + c < rows) {
+              const float gate = other, up = mine;
+              const float hv = gate / (1.0f + expf(-gate)) * up;
+              hp[(size_t)(start + c0 + c) * p.I + i] = __float2bfloat16_rn(hv);
+            }
+          }
+        } else {
+          const int jrow = rb * 128 + q * 32 + lane;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c0 + c < rows) {
+              const int pair = p.sorted_pair[start + c0 + c];
+              p.ypart[(size_t)pair * p.H + jrow] = __uint_as_float(v[c]) * gsc * p.topk_w[pair];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce[ab]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int NMAX, int STAGES, int ACCB, bool FC1>
+cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
+  using C = Cfg<NMAX, STAGES, ACCB>;
+  auto* k = moe_gemm_kernel<NMAX, STAGES, ACCB, FC1>;
+  cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (rc != cudaSuccess) return rc;
+  k<<<num_sms, kThreads, C::kSmemBytes, stream>>>(tmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 256; }
+
+cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
+                        int num_sms, cudaStream_t stream) {
+  const bool fc1 = kind == GemmKind::kFc1;
+  if (sched == QMOE_SCHED_DECODE)
+    return fc1 ? run<32, 6, 2, true>(tmap_b, p, num_sms, stream)
+               : run<32, 6, 2, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<256, 3, 1, true>(tmap_b, p, num_sms, stream)
+             : run<256, 3, 1, false>(tmap_b, p, num_sms, stream);
+}
+
+}  // namespace qmoe

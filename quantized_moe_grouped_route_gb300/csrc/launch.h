@@ -1,0 +1,52 @@
+// Host-side launchers shared between the translation units of libqmoe (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qmoe {
+
+// route.cu
+constexpr int kRouteThreads = 512;
+size_t route_smem_bytes(int E);
+cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
+                         int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
+                         unsigned int* err, cudaStream_t stream);
+
+// misc.cu
+cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
+                          uint8_t* out_codes, uint8_t* out_scales, cudaStream_t stream);
+cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
+                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
+                           void* out, int num_sms, cudaStream_t stream);
+cudaError_t launch_selftest_dequant(uint16_t* out, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(unsigned int* err, long long limit_ns, cudaStream_t stream);
+
+// gemm.cu
+struct GemmParams {
+  const uint8_t* wcodes;      // repacked codes
+  const uint8_t* wscales;     // repacked scales
+  const float* gscale;        // [E]
+  const int32_t* tiles;       // [n_tiles][3]
+  const int32_t* n_tiles;     // [1]
+  int K;                      // contraction length
+  int nrb;                    // 128-row weight blocks per expert
+  // FC1 output: h [rows][I] bf16
+  void* h;
+  int I;
+  // FC2 output: ypart [pairs][H] fp32
+  float* ypart;
+  const int32_t* sorted_pair;
+  const float* topk_w;
+  int H;
+  unsigned int* err;
+};
+
+enum class GemmKind { kFc1, kFc2 };
+cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
+                        int num_sms, cudaStream_t stream);
+int gemm_tile_n(int sched);  // max pairs per tile for a schedule
+
+}  // namespace qmoe

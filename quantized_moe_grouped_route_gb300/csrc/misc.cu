@@ -1,0 +1,193 @@
+// Repack, activation gather, top_k combine and the diagnostic kernels.
+#include "common.cuh"
+#include "dequant.cuh"
+#include "launch.h"
+
+namespace qmoe {
+namespace {
+
+// Repacked layout, per (expert e, 128-row block rb, 128-wide K step ks):
+//   codes : 8192 bytes = [kk 0..3][row 0..127][16 bytes = 32 elements], each 4-byte
+//           word holding eight consecutive K elements in the pack_codes8 layout
+//   scales: 1024 bytes = [row 0..127][8 scale bytes of the step's 8 K blocks]
+// so one stage of the GEMM is two contiguous bulk copies, and each dequant thread
+// (one weight row) reads its 16-byte chunks and its 8 scale bytes without shared
+// memory bank conflicts.
+__global__ void repack_codes_kernel(const uint8_t* __restrict__ w, int E, int N, int K, int w13,
+                                    uint32_t* __restrict__ out) {
+  const int nrb = N / 128, nks = K / 128;
+  const long long total = (long long)E * N * (K / 8);
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int wd = (int)(idx & 3);
+    const int r = (int)((idx >> 2) & 127);
+    long long rest = idx >> 9;
+    const int kk = (int)(rest & 3);
+    rest >>= 2;
+    const int ks = (int)(rest % nks);
+    rest /= nks;
+    const int rb = (int)(rest % nrb);
+    const int e = (int)(rest / nrb);
+    const int n = repack_row(w13 != 0, N, rb, r);
+    const int k0 = ks * 128 + kk * 32 + wd * 8;
+    const uint32_t plain =
+        *reinterpret_cast<const uint32_t*>(w + ((size_t)e * N + n) * (size_t)(K / 2) + k0 / 2);
+    out[idx] = pack_codes8(plain);
+  }
+}
+
+__global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N, int K, int w13,
+                                     uint2* __restrict__ out) {
+  const int nrb = N / 128, nks = K / 128;
+  const long long total = (long long)E * N * nks;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(idx & 127);
+    long long rest = idx >> 7;
+    const int ks = (int)(rest % nks);
+    rest /= nks;
+    const int rb = (int)(rest % nrb);
+    const int e = (int)(rest / nrb);
+    const int n = repack_row(w13 != 0, N, rb, r);
+    out[idx] = *reinterpret_cast<const uint2*>(s + ((size_t)e * N + n) * (size_t)(K / 16) + ks * 8);
+  }
+}
+
+// xs[pos] = x[sorted_pair[pos] / top_k] for the n_valid routed pairs (16-byte chunks).
+__global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pair,
+                              const int32_t* __restrict__ n_valid_p, int top_k, int chunks,
+                              uint4* __restrict__ xs) {
+  const long long total = (long long)(*n_valid_p) * chunks;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int pos = (int)(idx / chunks);
+    const int c = (int)(idx - (long long)pos * chunks);
+    const int tok = sorted_pair[pos] / top_k;
+    xs[idx] = x[(size_t)tok * chunks + c];
+  }
+}
+
+// out[m][j] = bf16( sum over k ascending of ypart[m*top_k + k][j] ) over the slots
+// whose expert id is in [0, E) (megamoe_rm.cu page, combine).  Fixed order, no
+// atomics: deterministic.  8 columns per thread.
+__global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ ids,
+                               int M, int top_k, int E, int H, uint4* __restrict__ out) {
+  const int c8 = H / 8;
+  const long long total = (long long)M * c8;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(idx / c8);
+    const int j0 = (int)(idx - (long long)m * c8) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < top_k; ++k) {
+      const int e = ids[m * top_k + k];
+      if (e < 0 || e >= E) continue;
+      const float4* src = reinterpret_cast<const float4*>(ypart + ((size_t)m * top_k + k) * H + j0);
+      const float4 a = src[0], b = src[1];
+      acc[0] += a.x;
+      acc[1] += a.y;
+      acc[2] += a.z;
+      acc[3] += a.w;
+      acc[4] += b.x;
+      acc[5] += b.y;
+      acc[6] += b.z;
+      acc[7] += b.w;
+    }
+    uint4 o;
+    __nv_bfloat162 t0 = __floats2bfloat162_rn(acc[0], acc[1]);
+    __nv_bfloat162 t1 = __floats2bfloat162_rn(acc[2], acc[3]);
+    __nv_bfloat162 t2 = __floats2bfloat162_rn(acc[4], acc[5]);
+    __nv_bfloat162 t3 = __floats2bfloat162_rn(acc[6], acc[7]);
+    o.x = *reinterpret_cast<uint32_t*>(&t0);
+    o.y = *reinterpret_cast<uint32_t*>(&t1);
+    o.z = *reinterpret_cast<uint32_t*>(&t2);
+    o.w = *reinterpret_cast<uint32_t*>(&t3);
+    out[idx] = o;
+  }
+}
+
+// Every (code, scale) pair through the GEMM's dequant path.
+__global__ void selftest_dequant_kernel(uint16_t* __restrict__ out) {
+  const int sb = blockIdx.x;  // scale byte
+  const int c = threadIdx.x;  // 0..15
+  if (c >= 16) return;
+  const uint32_t s2 = e4m3_scale_bf16x2(sb);
+  // put code c at element position (c % 8) of a word, zeros elsewhere
+  const int pos = c & 7;
+  const uint32_t plain = (uint32_t)c << (4 * pos);
+  uint32_t o[4];
+  dequant8(pack_codes8(plain), s2, o);
+  const uint32_t word = o[pos >> 1];
+  const uint16_t v = (pos & 1) ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFF);
+  // undo the 2^-7 the kernels fold into the epilogue: multiply by 128 exactly
+  const float f = __bfloat162float(__ushort_as_bfloat16(v)) * 128.0f;
+  out[c * 256 + sb] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// One bounded wait on a barrier that nothing ever arrives at.
+__global__ void selftest_timeout_kernel(unsigned int* err, long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+  }
+  __syncthreads();
+}
+
+int grid_for(long long work, int threads, int num_sms) {
+  long long b = (work + threads - 1) / threads;
+  long long cap = (long long)num_sms * 8;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
+                          uint8_t* out_codes, uint8_t* out_scales, cudaStream_t stream) {
+  const long long words = (long long)E * N * (K / 8);
+  const long long rows = (long long)E * N * (K / 128);
+  repack_codes_kernel<<<grid_for(words, 256, 1184), 256, 0, stream>>>(
+      w, E, N, K, w13 ? 1 : 0, reinterpret_cast<uint32_t*>(out_codes));
+  cudaError_t rc = cudaGetLastError();
+  if (rc != cudaSuccess) return rc;
+  repack_scales_kernel<<<grid_for(rows, 256, 1184), 256, 0, stream>>>(
+      s, E, N, K, w13 ? 1 : 0, reinterpret_cast<uint2*>(out_scales));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
+                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream) {
+  const int chunks = H / 8;
+  gather_kernel<<<grid_for((long long)P * chunks, 256, num_sms), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(x), sorted_pair, n_valid, top_k, chunks,
+      reinterpret_cast<uint4*>(xs));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
+                           void* out, int num_sms, cudaStream_t stream) {
+  const long long work = (long long)M * (H / 8);
+  combine_kernel<<<grid_for(work, 256, num_sms), 256, 0, stream>>>(
+      ypart, ids, M, top_k, E, H, reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_dequant(uint16_t* out, cudaStream_t stream) {
+  selftest_dequant_kernel<<<256, 32, 0, stream>>>(out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_timeout(unsigned int* err, long long limit_ns, cudaStream_t stream) {
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,178 @@
+// route_sort: group the (token, expert) pairs by expert.
+//
+// Definition (megamoe_rm.cu page, route_prep): a pair's slot is its rank among
+// earlier pairs with the same expert; pairs with expert -1 are skipped.  Offsets
+// per expert follow the "total tokens including expert" prefix of cutlass
+// discussion 2855.  The tile list cuts each expert's run of positions into tiles of
+// at most tile_n pairs, experts ascending.
+//
+// One block of 16 warps.  Each warp owns a contiguous range of pairs, so ranks come
+// out stable without any ordering between warps:
+//   A. warp-aggregated histogram: lanes with equal expert ids find each other with
+//      match.any, the lowest such lane adds the group size to the warp's own row
+//      of a [16][E] count table (no atomics, no races);
+//   B. block scan: per-expert totals, an exclusive scan over experts (offsets), an
+//      exclusive scan of tile counts, and each warp's starting position per expert;
+//   C. scatter: each warp walks its range again; a pair's position is its warp's
+//      running base for the expert plus its rank among equal lanes of the step.
+#include "common.cuh"
+#include "launch.h"
+
+namespace qmoe {
+namespace {
+
+constexpr int kWarps = kRouteThreads / 32;
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive prefix and
+// writes the block total to *total.  `scratch` holds kWarps ints.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) scratch[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < kWarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += t;
+    }
+    if (lane < kWarps) scratch[lane] = s;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int excl = incl - v + (w ? scratch[w - 1] : 0);
+  *total = scratch[kWarps - 1];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const int32_t* __restrict__ ids, int P, int E, int T, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_pos,
+                 int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
+                 unsigned int* __restrict__ err) {
+  extern __shared__ int hist[];  // [kWarps][E]
+  __shared__ int scan_scratch[kWarps];
+  __shared__ int s_total;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = 0;
+  __syncthreads();
+
+  // contiguous range per warp, a whole number of 32-pair steps
+  const int chunk = (((P + kWarps - 1) / kWarps) + 31) & ~31;
+  const int lo = w * chunk;
+  const int hi = min(P, lo + chunk);
+  int* hw = hist + w * E;
+  bool bad = false;
+
+  // A. warp-aggregated histogram
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    int e = -1;
+    if (i < hi) {
+      e = ids[i];
+      if (e >= E) {
+        bad = true;
+        e = -1;
+      }
+      if (e < 0) e = -1;
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(m) - 1) hw[e] += __popc(m);
+    __syncwarp();
+  }
+  if (bad) atomicOr(err, QMOE_FLAG_BAD_ID);
+  __syncthreads();
+
+  // B. totals, offsets, tile counts, per-warp bases.  Thread t owns experts
+  // [t*ept, (t+1)*ept).
+  const int ept = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = tid * ept;
+  int my_pairs = 0, my_tiles = 0;
+  for (int j = 0; j < ept; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      int c = 0;
+      for (int ww = 0; ww < kWarps; ++ww) c += hist[ww * E + e];
+      my_pairs += c;
+      my_tiles += (c + T - 1) / T;
+    }
+  }
+  int total_pairs, total_tiles;
+  int pair_base = block_exclusive_scan(my_pairs, scan_scratch, &total_pairs);
+  int tile_base = block_exclusive_scan(my_tiles, scan_scratch, &total_tiles);
+  for (int j = 0; j < ept; ++j) {
+    const int e = e0 + j;
+    if (e >= E) break;
+    offsets[e] = pair_base;
+    int run = pair_base;
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const int c = hist[ww * E + e];
+      hist[ww * E + e] = run;  // becomes warp ww's next position for expert e
+      run += c;
+    }
+    const int cnt = run - pair_base;
+    for (int s = 0; s < cnt; s += T) {
+      tiles[3 * tile_base + 0] = e;
+      tiles[3 * tile_base + 1] = pair_base + s;
+      tiles[3 * tile_base + 2] = min(T, cnt - s);
+      ++tile_base;
+    }
+    pair_base = run;
+  }
+  if (tid == 0) {
+    offsets[E] = total_pairs;
+    *n_tiles = total_tiles;
+    s_total = total_pairs;
+  }
+  __syncthreads();
+
+  // C. stable scatter
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    int e = -1;
+    if (i < hi) {
+      e = ids[i];
+      if (e >= E || e < 0) e = -1;
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    const int b = e >= 0 ? hw[e] : 0;
+    const int pos = b + __popc(m & lt_mask);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) hw[e] = b + __popc(m);
+    __syncwarp();
+    if (i < hi) {
+      if (e >= 0) {
+        sorted_pair[pos] = i;
+        pair_pos[i] = pos;
+      } else {
+        pair_pos[i] = -1;
+      }
+    }
+  }
+  for (int pos = s_total + tid; pos < P; pos += kRouteThreads) sorted_pair[pos] = -1;
+}
+
+}  // namespace
+
+size_t route_smem_bytes(int E) { return (size_t)kWarps * (size_t)E * sizeof(int); }
+
+cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
+                         int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
+                         unsigned int* err, cudaStream_t stream) {
+  const size_t smem = route_smem_bytes(E);
+  cudaError_t rc = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem);
+  if (rc != cudaSuccess) return rc;
+  route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, P, E, tile_n, offsets, sorted_pair, pair_pos,
+                                                   tiles, n_tiles, err);
+  return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,74 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports every
+symbol include/qmoe.h declares, answers the size queries, and rejects bad
+arguments before touching the device."""
+
+import ctypes
+
+import pytest
+
+from quantized_moe_grouped_route_gb300 import qmoe
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_moe_grouped_route_gb300 import build
+    build.build()
+    return qmoe.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = qmoe.exported_symbols()
+    assert "moe_route" in names and "moe_nvfp4_forward" in names and "moe_nvfp4_repack" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_size_queries(lib):
+    assert qmoe.qmoe_max_tiles(16, 8, 256, 32) == 4 + 256
+    assert qmoe.qmoe_max_tiles(8192, 8, 256, 256) == 256 + 256
+    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 16, 8, 256) == 32
+    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 8192, 8, 256) == 256
+    assert qmoe.qmoe_repacked_fp4_size(256, 4096, 7168) == 256 * 4096 * 3584
+    assert qmoe.qmoe_repacked_scale_size(256, 7168, 2048) == 256 * 7168 * 128
+    ws = qmoe.qmoe_forward_workspace_size(8192, 7168, 2048, 256, 8)
+    P = 8192 * 8
+    # gathered activations, h and fp32 partials dominate
+    assert ws >= P * 7168 * 2 + P * 2048 * 2 + P * 7168 * 4
+    assert qmoe.qmoe_forward_workspace_size(4, 100, 128, 8, 2) == 0  # bad shape
+
+
+def test_bad_arguments_are_rejected_before_any_device_work(lib):
+    null = ctypes.c_void_p(0)
+    # H not a multiple of 128
+    rc = lib.moe_nvfp4_forward(null, null, null, null, null, null, null, null, null, null,
+                               4, 100, 128, 8, 2, 0, null, 0, null)
+    assert rc == qmoe.QMOE_ERR_SHAPE
+    # E out of range
+    rc = lib.moe_nvfp4_forward(null, null, null, null, null, null, null, null, null, null,
+                               4, 128, 128, 0, 2, 0, null, 0, null)
+    assert rc == qmoe.QMOE_ERR_SHAPE
+    # null pointers
+    rc = lib.moe_nvfp4_forward(null, null, null, null, null, null, null, null, null, null,
+                               4, 128, 128, 8, 2, 0, null, 0, null)
+    assert rc == qmoe.QMOE_ERR_ARG
+    # bad schedule
+    rc = lib.moe_nvfp4_forward(null, null, null, null, null, null, null, null, null, null,
+                               4, 128, 128, 8, 2, 7, null, 0, null)
+    assert rc == qmoe.QMOE_ERR_ARG
+    # zero tokens is a no-op that succeeds without touching anything
+    rc = lib.moe_nvfp4_forward(null, null, null, null, null, null, null, null, null, null,
+                               0, 128, 128, 8, 2, 0, null, 0, null)
+    assert rc == qmoe.QMOE_OK
+    # repack: bad role, bad shape
+    assert lib.moe_nvfp4_repack(null, null, 1, 128, 128, 3, null, null, null) == qmoe.QMOE_ERR_ARG
+    assert lib.moe_nvfp4_repack(null, null, 1, 100, 128, 1, null, null, null) == qmoe.QMOE_ERR_SHAPE
+    # route: bad tile height, null outputs
+    assert lib.moe_route(null, 4, 2, 8, 0, null, null, null, null, null, null, 256, null) == \
+        qmoe.QMOE_ERR_SHAPE
+    assert lib.moe_route(null, 4, 2, 8, 16, null, null, null, null, null, null, 256, null) == \
+        qmoe.QMOE_ERR_ARG
+    # error-word read and diagnostics with null pointers
+    flags = ctypes.c_uint32(0)
+    assert lib.qmoe_read_error(null, null, ctypes.byref(flags)) == qmoe.QMOE_ERR_ARG
+    assert lib.qmoe_selftest_dequant(null, null) == qmoe.QMOE_ERR_ARG
+    assert lib.qmoe_selftest_timeout(null, 1000000, null) == qmoe.QMOE_ERR_ARG

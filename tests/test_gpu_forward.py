@@ -1,0 +1,94 @@
+"""GPU parity of the whole layer (moe_nvfp4_forward through the C-ABI) against the
+CPU oracle: small shapes element by element, the five workload configs at full
+size on sampled tokens (the benchmark's launch configuration), edge cases and
+determinism.  Tolerance per element: |got - ref| <= 2e-2 |ref| + 2e-3 rms(ref)."""
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_moe_grouped_route_gb300 import qmoe
+from qmoe_inputs import CONFIGS, LayerConfig, make_inputs
+from tests.helpers import check_close, gpu_forward, oracle_forward, to_np_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = [qmoe.QMOE_SCHED_DECODE, qmoe.QMOE_SCHED_PREFILL, qmoe.QMOE_SCHED_AUTO]
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_tiny_config_all_tokens(sched):
+    li = make_inputs(CONFIGS[0], "cpu").to("cuda")
+    out, _ = gpu_forward(li, sched)
+    check_close(to_np_bf16_bits(out), oracle_forward(li), f"tiny sched={sched}")
+
+
+SMALL = [
+    # name, M, H, I, E, top_k: several tiles per expert, ragged tails, one expert
+    ("m37_h256_i256_e5_k3", 37, 256, 256, 5, 3),
+    ("m300_h384_i128_e3_k2", 300, 384, 128, 3, 2),
+    ("m70_h128_i384_e1_k1", 70, 128, 384, 1, 1),
+    ("m129_h512_i256_e16_k4", 129, 512, 256, 16, 4),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s[0])
+@pytest.mark.parametrize("sched", SCHEDS[:2])
+def test_small_shapes_all_tokens(shape, sched):
+    name, M, H, I, E, k = shape
+    li = make_inputs(LayerConfig(name, M, H, I, E, k, seed=17), "cpu").to("cuda")
+    # some slots without an expert
+    ids = li.topk_ids.clone()
+    ids[::7, 0] = -1
+    li.topk_ids = ids.contiguous()
+    out, _ = gpu_forward(li, sched)
+    check_close(to_np_bf16_bits(out), oracle_forward(li), f"{name} sched={sched}")
+
+
+def test_duplicate_experts_and_bad_ids():
+    cfg = LayerConfig("dup", 24, 256, 128, 4, 3, seed=5)
+    li = make_inputs(cfg, "cpu").to("cuda")
+    ids = li.topk_ids.clone()
+    ids[:, 1] = ids[:, 0]           # the same expert twice in a token
+    ids[3, 2] = 9                   # >= E: skipped and flagged
+    ids[5, 2] = -1
+    li.topk_ids = ids.contiguous()
+    out, layer = gpu_forward(li, qmoe.QMOE_SCHED_AUTO)
+    rc, flags = qmoe.qmoe_read_error(layer._ws)
+    assert rc == qmoe.QMOE_ERR_BAD_ID and flags & qmoe.QMOE_FLAG_BAD_ID
+    # the oracle skips ids >= E as well
+    check_close(to_np_bf16_bits(out), oracle_forward(li), "duplicates")
+
+
+def _sample_tokens(M, n, seed):
+    if M <= n:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    s = np.sort(rng.choice(M, size=n - 2, replace=False))
+    return np.unique(np.concatenate([[0, M - 1], s]))
+
+
+@pytest.mark.parametrize("cfg", CONFIGS[1:], ids=lambda c: c.name)
+def test_full_config_sampled_tokens(cfg):
+    li = make_inputs(cfg, "cuda")
+    torch.cuda.synchronize()
+    out, layer = gpu_forward(li, qmoe.QMOE_SCHED_AUTO)
+    rc, flags = qmoe.qmoe_read_error(layer._ws)
+    assert rc == 0 and flags == 0
+    toks = _sample_tokens(cfg.M, 24, cfg.seed)
+    got = to_np_bf16_bits(out)[toks]
+    ref = oracle_forward(li, tokens=toks)
+    check_close(got, ref, cfg.name)
+    # deterministic: a second call is bitwise equal
+    out2, _ = gpu_forward(li, qmoe.QMOE_SCHED_AUTO, layer)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_zero_tokens_is_a_noop():
+    li = make_inputs(CONFIGS[0], "cpu").to("cuda")
+    layer = qmoe.NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
+    x = torch.empty(0, li.cfg.H, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(0, 2, dtype=torch.int32, device="cuda")
+    w = torch.empty(0, 2, dtype=torch.float32, device="cuda")
+    out = layer(x, ids, w)
+    assert out.shape == (0, li.cfg.H)
