@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--sched", choices=["auto", "decode", "prefill"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-soak", action="store_true",
+                    help="skip the untimed clock-sampling soak (for profiler launch lists)")
     return ap.parse_args()
 
 
@@ -181,7 +183,7 @@ def reference_arm(args, rank, world):
         return 0
     import torch
 
-    from qmoe_inputs import config_by_name, make_inputs
+    from qmoe_inputs.gen import config_by_name, make_inputs
     import oracle
     cfg = config_by_name(args.config)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -217,7 +219,7 @@ def ours_arm(args, rank, world, local):
     import torch.distributed as dist
 
     from quantized_moe_grouped_route_gb300 import NVFP4MoE, qmoe
-    from qmoe_inputs import config_by_name, make_inputs
+    from qmoe_inputs.gen import config_by_name, make_inputs
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -262,7 +264,7 @@ def ours_arm(args, rank, world, local):
     sampler = ClockSampler(local)
     sampler.start()
     t_soak = time.time()
-    while time.time() - t_soak < 0.6:  # let the sampler see the GPU under this load
+    while not args.no_soak and time.time() - t_soak < 0.6:  # let the sampler see the GPU under this load
         for _ in range(20):
             step()
         torch.cuda.synchronize()

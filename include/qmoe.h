@@ -134,6 +134,20 @@ int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8
                       size_t ws_bytes, void* stream);
 
 /*
+ * qmoe_forward_workspace_layout — byte offsets, inside a forward workspace, of what
+ * moe_nvfp4_forward leaves there, for inspection by tests and tools:
+ *   layout_out[0] offsets [E+1] int32      [1] sorted_pair [M*top_k] int32
+ *   layout_out[2] pair_pos [M*top_k] int32 [3] tiles [max_tiles][3] int32
+ *   layout_out[4] n_tiles int32            [5] xs: gathered x rows [rows][H] bf16
+ *   layout_out[6] h [rows][I] bf16, row = a pair's sorted position
+ *   layout_out[7] ypart [M*top_k][H] fp32, row = pair index
+ *   layout_out[8] total bytes              [9] rows (M*top_k rounded up to 16)
+ * layout_out must hold 10 entries.  (An inspection aid; no counterpart on the pages.)
+ */
+int qmoe_forward_workspace_layout(int M, int H, int I, int E, int top_k, int sched,
+                                  size_t* layout_out);
+
+/*
  * moe_nvfp4_forward_events — moe_nvfp4_forward that also records six caller-owned
  * cudaEvent_t at its stage boundaries on `stream`, so that each kernel can be timed
  * on the stream it runs on: events[0] before route, [1] after route, [2] after the

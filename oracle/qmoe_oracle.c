@@ -172,6 +172,31 @@ static double wq(const uint8_t* w, const uint8_t* s, int64_t K, int64_t n, int64
   return qo_dec_e2m1(code) * qo_dec_e4m3(s[n * (K / 16) + k / 16]);
 }
 
+/* Adjacent bf16 bit patterns towards +infinity / -infinity (finite inputs). */
+static uint16_t bf16_next_up(uint16_t b) {
+  if ((b & 0x7FFF) == 0) return 0x0001;
+  return (b & 0x8000) ? (uint16_t)(b - 1) : (uint16_t)(b + 1);
+}
+static uint16_t bf16_next_down(uint16_t b) {
+  if ((b & 0x7FFF) == 0) return 0x8001;
+  return (b & 0x8000) ? (uint16_t)(b + 1) : (uint16_t)(b - 1);
+}
+
+/* The two bf16 values bracketing v (lo <= v <= hi; both equal v when v is a bf16 value). */
+static void bf16_bracket(double v, double* lo, double* hi) {
+  uint16_t b = qo_bf16_rne(v);
+  double r = qo_bf16_to_double(b);
+  if (r == v) {
+    *lo = *hi = r;
+  } else if (r < v) {
+    *lo = r;
+    *hi = qo_bf16_to_double(bf16_next_up(b));
+  } else {
+    *hi = r;
+    *lo = qo_bf16_to_double(bf16_next_down(b));
+  }
+}
+
 /*
  * The layer for a subset of tokens (all of them when tokens == NULL):
  *   for each slot k of token m with expert e = ids[m][k] in [0, E):
@@ -182,12 +207,23 @@ static double wq(const uint8_t* w, const uint8_t* s, int64_t K, int64_t n, int64
  * x is bf16 bits [M][H]; weights are the plain row-major NVFP4 tensors
  * w13 [E][2I][H/2], s13 [E][2I][H/16], w2 [E][H][I/2], s2 [E][H][I/16].
  * out_bf16 / out_f64 are [n_tokens][H] (out_f64 may be NULL).
+ *
+ * Rounding h to bf16 is a decision taken on a floating-point value; a GPU that
+ * forms silu(gate) * up in fp32 may land on the other side of a rounding midpoint
+ * when the exact value is within its rounding noise of one.  qo_forward_h accepts
+ * such decisions from the caller: h_given ([n_tokens * top_k][I] bf16 bits, row
+ * t * top_k + k for the t-th listed token) replaces the oracle's own rounding, after
+ * each given value is checked to be one of the two bf16 values bracketing the exact
+ * silu(gate) * up.  h_stats (may be NULL) receives {values compared, values that
+ * differ from the oracle's own rounding, values outside the bracket}.  h_out (may be
+ * NULL, same layout as h_given) receives the h values used; rows of slots without an
+ * expert are zero.
  */
-int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
-               const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
-               const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
-               const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
-               int nthreads) {
+int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
+                 const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
+                 const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
+                 const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
+                 int nthreads, const uint16_t* h_given, int64_t* h_stats, uint16_t* h_out) {
   if (M < 0 || H < 16 || I < 16 || H % 16 || I % 16 || E < 1 || top_k < 1) return QO_ERR_ARG;
   if (tokens == NULL) n_tokens = M;
   for (int64_t t = 0; t < n_tokens; ++t) {
@@ -195,8 +231,9 @@ int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const 
     if (m < 0 || m >= M) return QO_ERR_ARG;
   }
   int bad_id = 0, nan_scale = 0;
+  int64_t n_cmp = 0, n_flip = 0, n_out = 0;
   if (nthreads < 1) nthreads = 1;
-#pragma omp parallel num_threads(nthreads)
+#pragma omp parallel num_threads(nthreads) reduction(+ : n_cmp, n_flip, n_out)
   {
     double* g = (double*)malloc(sizeof(double) * (size_t)(2 * I));
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
@@ -207,6 +244,8 @@ int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const 
       for (int64_t j = 0; j < H; ++j) acc[j] = 0.0;
       for (int k = 0; k < top_k; ++k) {
         int e = ids[m * top_k + k];
+        if (h_out)
+          for (int64_t i = 0; i < I; ++i) h_out[(t * top_k + k) * I + i] = 0;
         if (e < 0) continue;
         if (e >= E) {
           bad_id = 1;
@@ -223,7 +262,18 @@ int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const 
         for (int64_t i = 0; i < I; ++i) {
           double up = g[i], gate = g[I + i];
           double silu = gate / (1.0 + exp(-gate));
-          h[i] = qo_bf16_to_double(qo_bf16_rne(silu * up));
+          double exact = silu * up;
+          h[i] = qo_bf16_to_double(qo_bf16_rne(exact));
+          if (h_given) {
+            double given = qo_bf16_to_double(h_given[(t * top_k + k) * I + i]);
+            double lo, hi;
+            bf16_bracket(exact, &lo, &hi);
+            n_cmp += 1;
+            if (given != h[i]) n_flip += 1;
+            if (!(given == lo || given == hi)) n_out += 1;
+            h[i] = given;
+          }
+          if (h_out) h_out[(t * top_k + k) * I + i] = qo_bf16_rne(h[i]);
         }
         const uint8_t* w2e = w2 + (int64_t)e * H * (I / 2);
         const uint8_t* s2e = s2 + (int64_t)e * H * (I / 16);
@@ -244,8 +294,22 @@ int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const 
     free(h);
     free(acc);
   }
+  if (h_stats) {
+    h_stats[0] = n_cmp;
+    h_stats[1] = n_flip;
+    h_stats[2] = n_out;
+  }
   if (nan_scale) return QO_ERR_NAN_SCALE;
   return bad_id ? QO_WARN_BAD_ID : QO_OK;
+}
+
+int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
+               const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
+               const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
+               const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
+               int nthreads) {
+  return qo_forward_h(x, w13, s13, gs13, w2, s2, gs2, ids, topk_w, M, H, I, E, top_k, tokens,
+                      n_tokens, out_bf16, out_f64, nthreads, NULL, NULL, NULL);
 }
 
 /* Number of threads OpenMP would use by default (the host's cores). */

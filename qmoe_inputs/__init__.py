@@ -7,4 +7,5 @@ NVFP4 storage format (E2M1 nibbles, E4M3 block scales, fp32 global scale) that
 both sides then read byte for byte.
 """
 
-from .gen import CONFIGS, LayerConfig, LayerInputs, make_inputs, quantize_nvfp4  # noqa: F401
+from .gen import (CONFIGS, PROFILE_CONFIGS, LayerConfig, LayerInputs, config_by_name,  # noqa: F401
+                  make_inputs, quantize_nvfp4)

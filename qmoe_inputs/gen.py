@@ -50,6 +50,13 @@ CONFIGS = [
 ]
 
 
+# Smaller cases of the same kernels for profiler captures (inputs still larger than L2).
+PROFILE_CONFIGS = [
+    LayerConfig("decode_m16_h7168_i2048_e32_k8", 16, 7168, 2048, 32, 8, 1),
+    LayerConfig("prefill_m1024_h7168_i2048_e16_k8", 1024, 7168, 2048, 16, 8, 4),
+]
+
+
 @dataclasses.dataclass
 class LayerInputs:
     cfg: LayerConfig
@@ -171,7 +178,7 @@ def make_inputs(cfg: LayerConfig, device="cpu", seed: Optional[int] = None,
 
 
 def config_by_name(name: str) -> LayerConfig:
-    for c in CONFIGS:
+    for c in CONFIGS + PROFILE_CONFIGS:
         if c.name == name:
             return c
     raise KeyError(name)

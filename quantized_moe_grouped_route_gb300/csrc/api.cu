@@ -272,6 +272,19 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   return QMOE_OK;
 }
 
+int qmoe_forward_workspace_layout(int M, int H, int I, int E, int top_k, int sched,
+                                  size_t* layout_out) {
+  if (!layout_out) return QMOE_ERR_ARG;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL) return QMOE_ERR_ARG;
+  int rc = check_shape(M, H, I, E, top_k);
+  if (rc != QMOE_OK) return rc;
+  const ForwardLayout L = forward_layout(M, H, I, E, top_k, sched);
+  const size_t v[10] = {L.offsets, L.sorted_pair, L.pair_pos, L.tiles, L.n_tiles,
+                        L.xs,      L.h,           L.ypart,    L.total, (size_t)L.rows};
+  for (int i = 0; i < 10; ++i) layout_out[i] = v[i];
+  return QMOE_OK;
+}
+
 int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8_t* w13_scale_dev,
                       const float* w13_gscale_dev, const uint8_t* w2_fp4_dev,
                       const uint8_t* w2_scale_dev, const float* w2_gscale_dev,

@@ -74,6 +74,8 @@ def _bind(L):
                                     sz, P]),
         "moe_nvfp4_forward_events": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                            i32, P, sz, P, P]),
+        "qmoe_forward_workspace_layout": (i32, [i32, i32, i32, i32, i32, i32,
+                                                ctypes.POINTER(ctypes.c_size_t)]),
         "qmoe_read_error": (i32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
         "qmoe_selftest_dequant": (i32, [P, P]),
         "qmoe_selftest_timeout": (i32, [P, i64, P]),
@@ -128,6 +130,36 @@ def qmoe_route_workspace_size(M: int, top_k: int, E: int, tile_n: int) -> int:
 
 def qmoe_forward_workspace_size(M, H, I, E, top_k, sched=QMOE_SCHED_AUTO) -> int:
     return lib().qmoe_forward_workspace_size(M, H, I, E, top_k, sched)
+
+
+def qmoe_forward_workspace_layout(M, H, I, E, top_k, sched=QMOE_SCHED_AUTO) -> dict:
+    arr = (ctypes.c_size_t * 10)()
+    _check("qmoe_forward_workspace_layout",
+           lib().qmoe_forward_workspace_layout(M, H, I, E, top_k, sched, arr))
+    keys = ["offsets", "sorted_pair", "pair_pos", "tiles", "n_tiles", "xs", "h", "ypart", "total",
+            "rows"]
+    return dict(zip(keys, [int(v) for v in arr]))
+
+
+def workspace_views(ws: torch.Tensor, M, H, I, E, top_k, sched=QMOE_SCHED_AUTO) -> dict:
+    """Typed views of what a forward call left in its workspace (inspection only)."""
+    L = qmoe_forward_workspace_layout(M, H, I, E, top_k, sched)
+    P = M * top_k
+    rows = L["rows"]
+
+    def view(off, n, dtype):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[off:off + nbytes].view(dtype)
+
+    return {
+        "offsets": view(L["offsets"], E + 1, torch.int32),
+        "sorted_pair": view(L["sorted_pair"], P, torch.int32),
+        "pair_pos": view(L["pair_pos"], P, torch.int32),
+        "n_tiles": view(L["n_tiles"], 1, torch.int32),
+        "xs": view(L["xs"], rows * H, torch.bfloat16).view(rows, H),
+        "h": view(L["h"], rows * I, torch.bfloat16).view(rows, I),
+        "ypart": view(L["ypart"], P * H, torch.float32).view(P, H),
+    }
 
 
 def qmoe_repacked_fp4_size(E, N, K) -> int:

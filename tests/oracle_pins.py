@@ -215,37 +215,92 @@ def pin_zero_weights(lib):
     assert (out & 0x7FFF == 0).all()
 
 
-def pin_single_nibble(lib):
-    """One nonzero code per matrix: every factor of the output is known in closed form."""
+def _single_nibble_layer():
     rng = np.random.default_rng(1)
     M, H, I, E = 2, 64, 32, 3
     t = _zeros(M, H, I, E, 1)
     t["x"] = _rand_bf16(rng, (M, H))
     e, i0, j0 = 2, 5, 37
     ku, kg = 19, 42            # odd k -> high nibble, even k -> low nibble
-    cu, su = 0x5, 0x3A         # +3.0 ; 1.25
-    cg, sg = 0xC, 0x41         # -2.0 ; 2.25
-    c2, s2b = 0x7, 0x2C        # +6.0 ; 0.375
-    _set_code(t["w13"], t["s13"], e, i0, ku, cu, su)
-    _set_code(t["w13"], t["s13"], e, I + i0, kg, cg, sg)
-    _set_code(t["w2"], t["s2"], e, j0, i0, c2, s2b)
+    _set_code(t["w13"], t["s13"], e, i0, ku, 0x5, 0x3A)         # +3.0 ; 1.25
+    _set_code(t["w13"], t["s13"], e, I + i0, kg, 0xC, 0x41)     # -2.0 ; 2.25
+    _set_code(t["w2"], t["s2"], e, j0, i0, 0x7, 0x2C)           # +6.0 ; 0.375
     t["gs13"][:] = [7.0, 7.0, 0.75]
     t["gs2"][:] = [5.0, 5.0, 1.5]
     t["topk_ids"][:] = [[e], [e]]
     t["topk_weights"][:] = [[0.625], [-1.75]]
+    geo = dict(M=M, H=H, I=I, i0=i0, j0=j0, ku=ku, kg=kg)
+    return t, geo
+
+
+def _single_nibble_h(t, geo, m):
+    xu = bits_to_f(int(t["x"][m, geo["ku"]]))
+    xg = bits_to_f(int(t["x"][m, geo["kg"]]))
+    up = 0.75 * 3.0 * 1.25 * xu
+    gate = 0.75 * -2.0 * 2.25 * xg
+    return silu(gate) * up
+
+
+def pin_single_nibble(lib):
+    """One nonzero code per matrix: every factor of the output is known in closed form."""
+    t, geo = _single_nibble_layer()
     out = _run(lib, t)
-    for m in range(M):
-        xu = bits_to_f(int(t["x"][m, ku]))
-        xg = bits_to_f(int(t["x"][m, kg]))
-        up = 0.75 * 3.0 * 1.25 * xu
-        gate = 0.75 * -2.0 * 2.25 * xg
-        h = bits_to_f(brute_bf16(silu(gate) * up))
+    for m in range(geo["M"]):
+        h = bits_to_f(brute_bf16(_single_nibble_h(t, geo, m)))
         y = 1.5 * 6.0 * 0.375 * h
         want = brute_bf16(float(t["topk_weights"][m, 0]) * y)
-        for j in range(H):
-            expect = want if j == j0 else 0
-            mask = 0xFFFF if j == j0 else 0x7FFF
+        for j in range(geo["H"]):
+            expect = want if j == geo["j0"] else 0
+            mask = 0xFFFF if j == geo["j0"] else 0x7FFF
             assert (int(out[m, j]) & mask) == expect, (m, j, out[m, j], expect)
+
+
+def _bf16_neighbors(v):
+    """(lo, hi) bf16 bit patterns bracketing v, by brute force over all bf16 values."""
+    vals = all_bf16_values()
+    a = abs(v)
+    i = int(np.searchsorted(vals, a, side="right")) - 1   # largest value <= a
+    lo_mag, hi_mag = i, (i if vals[i] == a else i + 1)
+    sign = 0x8000 if v < 0 else 0
+    if v < 0:
+        lo_mag, hi_mag = hi_mag, lo_mag
+    return sign | lo_mag, sign | hi_mag
+
+
+def pin_h_given(lib):
+    """h decisions handed to the oracle: checked against the bracket of the exact value
+    and used for FC2 at the right index."""
+    t = _random_layer(21, M=4, H=64, I=32, E=3, top_k=2)
+    t["topk_ids"][1, 1] = -1
+    out, f64, info = _run(lib, t, return_f64=True, return_h=True)
+    n_valid = int((t["topk_ids"] >= 0).sum())
+    out2, f64b, st = _run(lib, t, return_f64=True, h_given=info["h"])
+    assert np.array_equal(out, out2) and np.array_equal(f64, f64b)
+    assert st["compared"] == n_valid * 32 and st["flipped"] == 0 and st["outside"] == 0
+    assert not info["h"][1 * 2 + 1].any()   # slot without an expert: zero row
+
+    t, geo = _single_nibble_layer()
+    I, i0, j0 = geo["I"], geo["i0"], geo["j0"]
+    for m_try in range(geo["M"]):
+        exact = _single_nibble_h(t, geo, m_try)
+        lo, hi = _bf16_neighbors(exact)
+        rne = brute_bf16(exact)
+        other = hi if rne == lo else lo
+        hg = np.zeros((geo["M"], I), np.uint16)
+        for m in range(geo["M"]):
+            hg[m, i0] = brute_bf16(_single_nibble_h(t, geo, m))
+        hg[m_try, i0] = other
+        o, st = _run(lib, t, h_given=hg)
+        assert st["compared"] == geo["M"] * I and st["flipped"] == 1 and st["outside"] == 0
+        y = 1.5 * 6.0 * 0.375 * bits_to_f(other)
+        assert int(o[m_try, j0]) == brute_bf16(float(t["topk_weights"][m_try, 0]) * y)
+        # two steps away from the exact value is not a valid rounding
+        far = (other + 1) if (other & 0x8000) == 0 and other == hi else other
+        if far == other:
+            far = (hi + 1) if (hi & 0x8000) == 0 else (hi - 1)
+        hg[m_try, i0] = far
+        _, st = _run(lib, t, h_given=hg)
+        assert st["outside"] == 1
 
 
 def pin_permutation_blocks(lib):
@@ -386,5 +441,5 @@ def pin_tiny_config(lib):
 
 
 ALL_PINS = [pin_e2m1, pin_e4m3, pin_bf16_decode, pin_bf16_round, pin_route, pin_zero_weights,
-            pin_single_nibble, pin_permutation_blocks, pin_subnormal_scale, pin_token_permutation,
+            pin_single_nibble, pin_h_given, pin_permutation_blocks, pin_subnormal_scale, pin_token_permutation,
             pin_duplicate_expert, pin_weight_linearity, pin_numpy_twin, pin_tiny_config]

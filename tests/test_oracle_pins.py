@@ -33,7 +33,10 @@ MUTANTS = {
     "gscale13_dropped": ("g[n] = (double)gs13[e] * sum;", "g[n] = sum;"),
     "gscale2_dropped": ("double y = (double)gs2[e] * sum;", "double y = sum;"),
     "scale_block_index": ("s[n * (K / 16) + k / 16]", "s[n * (K / 16) + k / 32]"),
-    "h_not_rounded": ("h[i] = qo_bf16_to_double(qo_bf16_rne(silu * up));", "h[i] = silu * up;"),
+    "h_not_rounded": ("h[i] = qo_bf16_to_double(qo_bf16_rne(exact));", "h[i] = exact;"),
+    "h_given_ignored": ("            h[i] = given;\n", "\n"),
+    "h_bracket_one_sided": ("if (!(given == lo || given == hi)) n_out += 1;", "if (!(given == lo)) n_out += 1;"),
+    "h_flip_uncounted": ("if (given != h[i]) n_flip += 1;", ";"),
     "routing_weight_dropped": ("acc[j] += (double)topk_w[m * top_k + k] * y;", "acc[j] += y;"),
     "e2m1_sign_dropped": ("return (code & 8) ? -m : m;", "return m;"),
     "e2m1_table": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 3.0, 3.5}"),
