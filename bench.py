@@ -271,6 +271,9 @@ def ours_arm(args, rank, world, local):
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:  # torch creates the CUDA event on first record
+        for ev in row:
+            ev.record()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()

@@ -209,13 +209,19 @@ static void bf16_bracket(double v, double* lo, double* hi) {
  * out_bf16 / out_f64 are [n_tokens][H] (out_f64 may be NULL).
  *
  * Rounding h to bf16 is a decision taken on a floating-point value; a GPU that
- * forms silu(gate) * up in fp32 may land on the other side of a rounding midpoint
+ * accumulates gate and up in fp32 may land on the other side of a rounding midpoint
  * when the exact value is within its rounding noise of one.  qo_forward_h accepts
  * such decisions from the caller: h_given ([n_tokens * top_k][I] bf16 bits, row
  * t * top_k + k for the t-th listed token) replaces the oracle's own rounding, after
- * each given value is checked to be one of the two bf16 values bracketing the exact
- * silu(gate) * up.  h_stats (may be NULL) receives {values compared, values that
- * differ from the oracle's own rounding, values outside the bracket}.  h_out (may be
+ * each given value is checked to be a valid rounding: the bf16 rounding of some value
+ * within delta of the exact silu(gate) * up, where delta is the first-order effect of
+ * fp32 accumulation errors on the two dot products,
+ *   d_up   = c * u * gs13 * sum_h |x[h] * Wq13[i][h]|        (likewise d_gate, row I+i)
+ *   delta  = |silu(gate)| * d_up + 1.1 * |up| * d_gate + 8 * u * |silu(gate) * up|
+ * with u = 2^-24 (fp32 unit roundoff), c = 2 * (H / 16 + 4) (one rounding per
+ * 16-wide MMA step of the accumulation, doubled), 1.1 >= max |SiLU'|.  h_stats (may
+ * be NULL) receives {values compared, values that differ from the oracle's own
+ * rounding, values that are not a valid rounding}.  h_out (may be
  * NULL, same layout as h_given) receives the h values used; rows of slots without an
  * expert are zero.
  */
@@ -236,8 +242,10 @@ int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, cons
 #pragma omp parallel num_threads(nthreads) reduction(+ : n_cmp, n_flip, n_out)
   {
     double* g = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* ga = (double*)malloc(sizeof(double) * (size_t)(2 * I));
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
     double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    const double u = ldexp(1.0, -24), c_acc = 2.0 * (double)(H / 16 + 4);
 #pragma omp for schedule(dynamic, 1)
     for (int64_t t = 0; t < n_tokens; ++t) {
       int64_t m = tokens ? tokens[t] : t;
@@ -254,10 +262,14 @@ int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, cons
         const uint8_t* we = w13 + (int64_t)e * (2 * I) * (H / 2);
         const uint8_t* se = s13 + (int64_t)e * (2 * I) * (H / 16);
         for (int64_t n = 0; n < 2 * I; ++n) {
-          double sum = 0.0;
-          for (int64_t hh = 0; hh < H; ++hh)
-            sum += qo_bf16_to_double(x[m * H + hh]) * wq(we, se, H, n, hh);
+          double sum = 0.0, asum = 0.0;
+          for (int64_t hh = 0; hh < H; ++hh) {
+            double term = qo_bf16_to_double(x[m * H + hh]) * wq(we, se, H, n, hh);
+            sum += term;
+            asum += fabs(term);
+          }
           g[n] = (double)gs13[e] * sum;
+          ga[n] = fabs((double)gs13[e]) * asum;
         }
         for (int64_t i = 0; i < I; ++i) {
           double up = g[i], gate = g[I + i];
@@ -266,11 +278,14 @@ int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, cons
           h[i] = qo_bf16_to_double(qo_bf16_rne(exact));
           if (h_given) {
             double given = qo_bf16_to_double(h_given[(t * top_k + k) * I + i]);
-            double lo, hi;
-            bf16_bracket(exact, &lo, &hi);
+            double delta = fabs(silu) * c_acc * u * ga[i] + 1.1 * fabs(up) * c_acc * u * ga[I + i] +
+                           8.0 * u * fabs(exact);
+            double lo, hi, lo2, hi2;
+            bf16_bracket(exact - delta, &lo, &hi2);
+            bf16_bracket(exact + delta, &lo2, &hi);
             n_cmp += 1;
             if (given != h[i]) n_flip += 1;
-            if (!(given == lo || given == hi)) n_out += 1;
+            if (!(given >= lo && given <= hi)) n_out += 1;
             h[i] = given;
           }
           if (h_out) h_out[(t * top_k + k) * I + i] = qo_bf16_rne(h[i]);
@@ -291,6 +306,7 @@ int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, cons
       }
     }
     free(g);
+    free(ga);
     free(h);
     free(acc);
   }

@@ -35,7 +35,7 @@ MUTANTS = {
     "scale_block_index": ("s[n * (K / 16) + k / 16]", "s[n * (K / 16) + k / 32]"),
     "h_not_rounded": ("h[i] = qo_bf16_to_double(qo_bf16_rne(exact));", "h[i] = exact;"),
     "h_given_ignored": ("            h[i] = given;\n", "\n"),
-    "h_bracket_one_sided": ("if (!(given == lo || given == hi)) n_out += 1;", "if (!(given == lo)) n_out += 1;"),
+    "h_bracket_one_sided": ("if (!(given >= lo && given <= hi)) n_out += 1;", "if (!(given >= lo)) n_out += 1;"),
     "h_flip_uncounted": ("if (given != h[i]) n_flip += 1;", ";"),
     "routing_weight_dropped": ("acc[j] += (double)topk_w[m * top_k + k] * y;", "acc[j] += y;"),
     "e2m1_sign_dropped": ("return (code & 8) ? -m : m;", "return m;"),
