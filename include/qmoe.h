@@ -134,6 +134,37 @@ int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8
                       size_t ws_bytes, void* stream);
 
 /*
+ * moe_nvfp4_forward_noalloc — moe_nvfp4_forward for callers that cannot allocate
+ * device memory: a plugin called from inside another runtime's enqueue step with no
+ * allocator handed to it, a C host program that does not own the process's memory
+ * pool, or a serving loop that must not allocate once it is running.  It takes the
+ * same inputs and outputs (all still passed in by the caller) but no workspace:
+ * it uses a scratch array of QMOE_NOALLOC_SCRATCH_BYTES (16 MiB) built into the
+ * library, which every GPU that loads the library holds until the process exits.
+ *  - Size limit: the batch must fit that array, i.e. qmoe_forward_workspace_size(
+ *    M, H, I, E, top_k, sched) <= QMOE_NOALLOC_SCRATCH_BYTES (decode-sized batches:
+ *    e.g. M = 16, H = 7168, I = 2048, top_k = 8 needs about 6 MB); larger batches get
+ *    QMOE_ERR_WORKSPACE before anything is enqueued.
+ *  - Set-up: the first call on a device, made with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call before any
+ *    stream capture.
+ *  - It calls no cudaMalloc / cudaFree and no allocating library routine.
+ *  - Every call shares the one array and leaves its contents behind; the error word
+ *    in it is cleared at the start of each call.  Calls that overlap on the GPU (on
+ *    different streams, or from several host threads) race on the array and give
+ *    wrong results: serialise them.  qmoe_read_error cannot see this array; a
+ *    bad-id or timeout flag from this call is not reported.
+ * The pages have no counterpart of this entry point.
+ */
+#define QMOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+int moe_nvfp4_forward_noalloc(const void* x_dev, const uint8_t* w13_fp4_dev,
+                              const uint8_t* w13_scale_dev, const float* w13_gscale_dev,
+                              const uint8_t* w2_fp4_dev, const uint8_t* w2_scale_dev,
+                              const float* w2_gscale_dev, const int32_t* topk_ids_dev,
+                              const float* topk_weights_dev, void* out_dev, int M, int H, int I,
+                              int E, int top_k, int sched, void* stream);
+
+/*
  * qmoe_forward_workspace_layout — byte offsets, inside a forward workspace, of what
  * moe_nvfp4_forward leaves there, for inspection by tests and tools:
  *   layout_out[0] offsets [E+1] int32      [1] sorted_pair [M*top_k] int32

@@ -107,6 +107,15 @@ ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA; }
 
+// Scratch for moe_nvfp4_forward_noalloc: a fixed array inside the library, so that
+// callers which cannot allocate device memory still have somewhere to put the
+// routing tables, gathered activations, h and per-pair partial outputs.  Every GPU
+// that loads the library holds it until the process exits.
+__device__ __align__(256) uint8_t g_noalloc_scratch[QMOE_NOALLOC_SCRATCH_BYTES];
+// Its device address per device, looked up on the first call made with that
+// device current (host code cannot use the symbol itself as a device pointer).
+void* g_noalloc_addr[kMaxDevices];
+
 }  // namespace
 }  // namespace qmoe
 
@@ -294,6 +303,32 @@ int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8
   return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
                       w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
                       sched, workspace_dev, ws_bytes, stream, nullptr);
+}
+
+int moe_nvfp4_forward_noalloc(const void* x_dev, const uint8_t* w13_fp4_dev,
+                              const uint8_t* w13_scale_dev, const float* w13_gscale_dev,
+                              const uint8_t* w2_fp4_dev, const uint8_t* w2_scale_dev,
+                              const float* w2_gscale_dev, const int32_t* topk_ids_dev,
+                              const float* topk_weights_dev, void* out_dev, int M, int H, int I,
+                              int E, int top_k, int sched, void* stream) {
+  int rc = check_shape(M, H, I, E, top_k);
+  if (rc != QMOE_OK) return rc;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL) return QMOE_ERR_ARG;
+  if (M == 0) return QMOE_OK;
+  if (forward_layout(M, H, I, E, top_k, sched).total > (size_t)QMOE_NOALLOC_SCRATCH_BYTES)
+    return QMOE_ERR_WORKSPACE;  // this batch needs more scratch than the built-in array
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMOE_ERR_CUDA;
+  if (!g_noalloc_addr[dev]) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
+      return QMOE_ERR_CUDA;
+    g_noalloc_addr[dev] = addr;
+  }
+  return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
+                      w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
+                      sched, g_noalloc_addr[dev], (size_t)QMOE_NOALLOC_SCRATCH_BYTES, stream,
+                      nullptr);
 }
 
 int moe_nvfp4_forward_events(const void* x_dev, const uint8_t* w13_fp4_dev,

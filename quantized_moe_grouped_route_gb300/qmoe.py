@@ -72,6 +72,8 @@ def _bind(L):
         "qmoe_forward_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "moe_nvfp4_forward": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
                                     sz, P]),
+        "moe_nvfp4_forward_noalloc": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                            i32, P]),
         "moe_nvfp4_forward_events": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                            i32, P, sz, P, P]),
         "qmoe_forward_workspace_layout": (i32, [i32, i32, i32, i32, i32, i32,
@@ -234,6 +236,26 @@ def moe_nvfp4_forward(x, w13_fp4, w13_scale, w13_gscale, w2_fp4, w2_scale, w2_gs
                                  _ptr(topk_weights), _ptr(out), M, H, I, E, top_k, sched,
                                  _ptr(workspace), workspace.numel(), _stream(stream))
     _check("moe_nvfp4_forward", rc)
+    return out
+
+
+# Size of the scratch array built into libqmoe for moe_nvfp4_forward_noalloc.
+QMOE_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def moe_nvfp4_forward_noalloc(x, w13_fp4, w13_scale, w13_gscale, w2_fp4, w2_scale, w2_gscale,
+                              topk_ids, topk_weights, out, *, H: int, I: int, E: int,
+                              sched: int = QMOE_SCHED_AUTO, stream=None) -> torch.Tensor:
+    """The layer without a caller workspace: the library's built-in scratch array is
+    used instead (for callers that cannot allocate device memory).  `out` must be
+    given; nothing is allocated."""
+    M = x.shape[0]
+    top_k = topk_ids.shape[1]
+    rc = lib().moe_nvfp4_forward_noalloc(
+        _ptr(x), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w13_gscale), _ptr(w2_fp4), _ptr(w2_scale),
+        _ptr(w2_gscale), _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, H, I, E, top_k, sched,
+        _stream(stream))
+    _check("moe_nvfp4_forward_noalloc", rc)
     return out
 
 
