@@ -11,9 +11,10 @@
 // batches still fill the instruction, and every output element is produced by one
 // CTA in a fixed order (deterministic, no split reduction).
 //
-// Data path per 128-wide K step (one pipeline stage):
-//   TMA warp      : bulk copy of the step's packed codes (8 KB) and scales (1 KB),
-//                   tiled TMA of the pair rows (bf16, 128-byte swizzle) -> smem ring
+// Data path per 128-wide K step (one pipeline step):
+//   TMA warps     : bulk copy of the step's packed codes (8 KB) and scales (1 KB)
+//                   into the weight ring; tiled TMA of the pair rows (bf16, 128-byte
+//                   swizzle) into the pair-row ring
 //   dequant warps : codes -> bf16 in registers (bit placement + one bf16x2 multiply
 //                   by the block scale) -> tcgen05.st into TMEM (the MMA's A operand)
 //   MMA thread    : 8 x tcgen05.mma kind::f16, A from TMEM, B from smem, fp32
@@ -33,24 +34,32 @@
 namespace qmoe {
 namespace {
 
-constexpr int kThreads = 448;       // 14 warps
-constexpr int kBK = 128;            // K per stage
+constexpr int kBK = 128;            // K per pipeline step
 constexpr int kCodeBytes = 8192;    // 128 rows x 128 K / 2
 constexpr int kScaleBytes = 1024;   // 128 rows x 8 blocks
+constexpr int kRawBytes = kCodeBytes + kScaleBytes;
 constexpr int kTmemCols = 512;
 constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale table
+constexpr int kWarps = 15;          // 0 codes TMA, 1 MMA, 2-5 epilogue, 6-13 dequant, 14 pair-row TMA
+constexpr int kThreads = kWarps * 32;
 
-template <int NMAX, int STAGES, int ACCB>
+// Three rings, each with its own depth:
+//   raw ring  (RS stages): packed codes + scales of one 128-wide K step, refilled as
+//             soon as the dequant warps have read it, so many weight bytes stay in
+//             flight per SM (the decode bound is HBM latency x bandwidth);
+//   B ring    (BS stages): the tile's pair rows for one K step, freed by the MMA;
+//   A slots   (AS in TMEM): dequantized bf16 weights, freed by the MMA.
+template <int NMAX, int RS, int BS, int AS, int ACCB>
 struct Cfg {
   static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
   static constexpr int kBBytes = 2 * kBSlab;
-  static constexpr int kStageBytes = kBBytes + kCodeBytes + kScaleBytes;
-  static constexpr int kAccCol0 = STAGES * 64;  // TMEM: [A slots: 64 cols each][accumulators]
-  static constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + kCtrlBytes;
-  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-  static_assert(STAGES * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
+  static constexpr int kAccCol0 = AS * 64;   // TMEM: [A slots: 64 cols each][accumulators]
+  static constexpr int kSmemBytes = BS * kBBytes + RS * kRawBytes + 1024 + kCtrlBytes;
+  static_assert(kBBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte stage alignment");
+  static_assert(AS * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(3 * (RS + BS + AS + ACCB) * 8 + 64 <= 1024, "barrier area");
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -61,18 +70,23 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int STAGES, int ACCB, bool FC1>
+template <int NMAX, int RS, int BS, int AS, int ACCB, bool FC1>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using C = Cfg<NMAX, STAGES, ACCB>;
+  using C = Cfg<NMAX, RS, BS, AS, ACCB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* ctrl = smem + STAGES * C::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);  // TMA bytes landed
-  uint64_t* deq = full + STAGES;                        // A slot written (4 warps)
-  uint64_t* empty = deq + STAGES;                       // MMA finished reading the stage
-  uint64_t* accf = empty + STAGES;                      // accumulator ready
+  uint8_t* bring = smem;                          // [BS][kBBytes]
+  uint8_t* rring = smem + BS * C::kBBytes;        // [RS][kRawBytes]
+  uint8_t* ctrl = rring + RS * kRawBytes;
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(ctrl);  // raw step landed (tx)
+  uint64_t* rempty = rfull + RS;                        // raw step read by 4 dequant warps
+  uint64_t* bfull = rempty + RS;                        // pair rows landed (tx)
+  uint64_t* bempty = bfull + BS;                        // pair rows read by the MMA
+  uint64_t* afull = bempty + BS;                        // A slot written by 4 dequant warps
+  uint64_t* aempty = afull + AS;                        // A slot read by the MMA
+  uint64_t* accf = aempty + AS;                         // accumulator ready
   uint64_t* acce = accf + ACCB;                         // accumulator drained (4 warps)
   uint64_t* drain = acce + ACCB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -81,10 +95,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&deq[s]), 4);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int s = 0; s < RS; ++s) {
+      mbar_init(smem_u32(&rfull[s]), 1);
+      mbar_init(smem_u32(&rempty[s]), 4);
+    }
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(smem_u32(&bfull[s]), 1);
+      mbar_init(smem_u32(&bempty[s]), 1);
+    }
+    for (int s = 0; s < AS; ++s) {
+      mbar_init(smem_u32(&afull[s]), 4);
+      mbar_init(smem_u32(&aempty[s]), 1);
     }
     for (int a = 0; a < ACCB; ++a) {
       mbar_init(smem_u32(&accf[a]), 1);
@@ -99,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_b);
+  if (warp == 14 && lane == 0) prefetch_tmap(&tmap_b);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -109,43 +130,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = (*p.n_tiles) * p.nrb;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ weight TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_b = l2_policy_evict_last();
+      const uint64_t pol = l2_policy_evict_first();
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int t = u / p.nrb, rb = u - t * p.nrb;
-        const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
-        const int nb16 = (rows + 15) >> 4;
-        const uint32_t tx = kCodeBytes + kScaleBytes + 2u * (uint32_t)nb16 * 2048u;
+        const int e = p.tiles[3 * t];
         const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nks;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, p.err)) {
+          const int s = it % RS;
+          if (!mbar_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * C::kStageBytes;
-          const uint32_t fb = smem_u32(&full[s]);
+          uint8_t* st = rring + s * kRawBytes;
+          const uint32_t fb = smem_u32(&rfull[s]);
+          mbar_arrive_expect_tx(fb, kRawBytes);
+          bulk_g2s(smem_u32(st), p.wcodes + (blk + ks) * kCodeBytes, kCodeBytes, fb, pol);
+          bulk_g2s(smem_u32(st + kCodeBytes), p.wscales + (blk + ks) * kScaleBytes, kScaleBytes, fb,
+                   pol);
+        }
+      }
+      if (!ok) {  // let the copies already issued land before the CTA can exit
+        const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
+        for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
+      }
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ pair-row TMA producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int t = u / p.nrb;
+        const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
+        const int nb16 = (rows + 15) >> 4;
+        const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % BS;
+          if (!mbar_wait(smem_u32(&bempty[s]), ((it / BS) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = bring + s * C::kBBytes;
+          const uint32_t fb = smem_u32(&bfull[s]);
           mbar_arrive_expect_tx(fb, tx);
-          bulk_g2s(smem_u32(st + C::kBBytes), p.wcodes + (blk + ks) * kCodeBytes, kCodeBytes, fb,
-                   pol_w);
-          bulk_g2s(smem_u32(st + C::kBBytes + kCodeBytes), p.wscales + (blk + ks) * kScaleBytes,
-                   kScaleBytes, fb, pol_w);
 #pragma unroll
           for (int sl = 0; sl < 2; ++sl)
             for (int g = 0; g < nb16; ++g)
               tma_load_2d(smem_u32(st + sl * C::kBSlab + g * 2048), &tmap_b, ks * kBK + sl * 64,
-                          start + g * 16, fb, pol_b);
+                          start + g * 16, fb, pol);
         }
       }
       if (!ok) {
-        // let the copies already issued land before the CTA can exit
-        const uint32_t first = it > (uint32_t)STAGES ? it - STAGES : 0u;
-        for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&full[j % STAGES]), (j / STAGES) & 1);
+        const uint32_t first = it > (uint32_t)BS ? it - BS : 0u;
+        for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&bfull[j % BS]), (j / BS) & 1);
       }
     }
   } else if (warp == 1) {
@@ -158,30 +200,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rows = p.tiles[3 * t + 2];
         const uint32_t idesc = idesc_bf16_f32(128, ((rows + 15) >> 4) << 4);
         const int ab = local % ACCB;
-        const uint32_t aph = (local / ACCB) & 1;
-        if (!mbar_wait(smem_u32(&acce[ab]), aph ^ 1, abort_flag, p.err)) {
+        if (!mbar_wait(smem_u32(&acce[ab]), ((local / ACCB) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err) ||
-              !mbar_wait(smem_u32(&deq[s]), ph, abort_flag, p.err)) {
+          const int a = it % AS, b = it % BS;
+          if (!mbar_wait(smem_u32(&bfull[b]), (it / BS) & 1, abort_flag, p.err) ||
+              !mbar_wait(smem_u32(&afull[a]), (it / AS) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b0 = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t b0 = smem_u32(bring + b * C::kBBytes);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t baddr = b0 + (j >> 2) * C::kBSlab + (j & 3) * 32;
-            mma_bf16_ts(d_tmem, tmem + s * 64 + j * 8, sdesc_sw128(baddr), idesc,
+            mma_bf16_ts(d_tmem, tmem + a * 64 + j * 8, sdesc_sw128(baddr), idesc,
                         (ks | j) != 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&empty[s]));
+          tc_commit(smem_u32(&aempty[a]));
+          tc_commit(smem_u32(&bempty[b]));
         }
         if (ok) tc_commit(smem_u32(&accf[ab]));
       }
@@ -190,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(smem_u32(drain), 0);
     }
   } else if (warp >= 6) {
-    // ------------------------------------------------------------ dequant warps
-    const int grp = (warp - 6) >> 2;  // which stages: it % 2 == grp
+    // ------------------------------------------------------------ dequant warps 6..13
+    const int grp = (warp - 6) >> 2;  // which steps: it % 2 == grp
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;    // weight row of the 128-row block
     uint32_t it = 0;
@@ -199,34 +240,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
         if ((int)(it & 1) != grp) continue;
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err)) {
+        const int s = it % RS, a = it % AS;
+        if (!mbar_wait(smem_u32(&rfull[s]), (it / RS) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint8_t* st = smem + s * C::kStageBytes;
-        const uint4* codes = reinterpret_cast<const uint4*>(st + C::kBBytes);
-        const uint2 sc = *reinterpret_cast<const uint2*>(st + C::kBBytes + kCodeBytes + row * 8);
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + s * 64;
+        const uint8_t* st = rring + s * kRawBytes;
+        const uint4* codes = reinterpret_cast<const uint4*>(st);
+        uint4 cw[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) cw[kk] = codes[kk * 128 + row];
+        const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + row * 8);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw step may be refilled
+        if (!mbar_wait(smem_u32(&aempty[a]), ((it / AS) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * 64;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint4 cw = codes[kk * 128 + row];
           const uint32_t sb = (kk < 2) ? sc.x : sc.y;
           const int sh = 16 * (kk & 1);
           const uint32_t s0 = scale_lut[(sb >> sh) & 0xFF];
           const uint32_t s1 = scale_lut[(sb >> (sh + 8)) & 0xFF];
           uint32_t o[16];
-          dequant8(cw.x, s0, o + 0);
-          dequant8(cw.y, s0, o + 4);
-          dequant8(cw.z, s1, o + 8);
-          dequant8(cw.w, s1, o + 12);
+          dequant8(cw[kk].x, s0, o + 0);
+          dequant8(cw[kk].y, s0, o + 4);
+          dequant8(cw[kk].z, s1, o + 8);
+          dequant8(cw[kk].w, s1, o + 12);
           tmem_st_x16(ta + kk * 16, o);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&deq[s]));
+        if (lane == 0) mbar_arrive(smem_u32(&afull[a]));
       }
     }
   } else {
@@ -237,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
-      const uint32_t aph = (local / ACCB) & 1;
-      if (!mbar_wait(smem_u32(&accf[ab]), aph, abort_flag, p.err)) break;
+      if (!mbar_wait(smem_u32(&accf[ab]), (local / ACCB) & 1, abort_flag, p.err)) break;
       tc_fence_after();
       const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMAX;
@@ -285,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NMAX, int STAGES, int ACCB, bool FC1>
+template <int NMAX, int RS, int BS, int AS, int ACCB, bool FC1>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
-  using C = Cfg<NMAX, STAGES, ACCB>;
-  auto* k = moe_gemm_kernel<NMAX, STAGES, ACCB, FC1>;
+  using C = Cfg<NMAX, RS, BS, AS, ACCB>;
+  auto* k = moe_gemm_kernel<NMAX, RS, BS, AS, ACCB, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   k<<<num_sms, kThreads, C::kSmemBytes, stream>>>(tmap, p);
@@ -299,14 +347,18 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 
 int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 256; }
 
+// decode : tiles <= 32 pairs, 14 weight steps in flight (126 KB), 8 pair-row steps,
+//          6 TMEM A slots, 2 accumulators
+// prefill: tiles <= 256 pairs, 8 weight steps, 2 pair-row steps (64 KB each),
+//          3 TMEM A slots, 1 accumulator (256 columns)
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
   if (sched == QMOE_SCHED_DECODE)
-    return fc1 ? run<32, 6, 2, true>(tmap_b, p, num_sms, stream)
-               : run<32, 6, 2, false>(tmap_b, p, num_sms, stream);
-  return fc1 ? run<256, 3, 1, true>(tmap_b, p, num_sms, stream)
-             : run<256, 3, 1, false>(tmap_b, p, num_sms, stream);
+    return fc1 ? run<32, 14, 8, 6, 2, true>(tmap_b, p, num_sms, stream)
+               : run<32, 14, 8, 6, 2, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<256, 8, 2, 3, 1, true>(tmap_b, p, num_sms, stream)
+             : run<256, 8, 2, 3, 1, false>(tmap_b, p, num_sms, stream);
 }
 
 }  // namespace qmoe
