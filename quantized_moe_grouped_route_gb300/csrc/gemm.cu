@@ -131,105 +131,106 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight TMA producer
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      uint32_t it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int t = u / p.nrb, rb = u - t * p.nrb;
-        const int e = p.tiles[3 * t];
-        const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nks;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % RS;
-          if (!mbar_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = rring + s * kRawBytes;
-          const uint32_t fb = smem_u32(&rfull[s]);
-          mbar_arrive_expect_tx(fb, kRawBytes);
-          bulk_g2s(smem_u32(st), p.wcodes + (blk + ks) * kCodeBytes, kCodeBytes, fb, pol);
-          bulk_g2s(smem_u32(st + kCodeBytes), p.wscales + (blk + ks) * kScaleBytes, kScaleBytes, fb,
-                   pol);
+    // (whole warp, converged; one elected lane issues)
+    const uint32_t leader = elect_one();
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int t = u / p.nrb, rb = u - t * p.nrb;
+      const int e = p.tiles[3 * t];
+      const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nks;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int s = it % RS;
+        if (!warp_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
         }
+        const uint32_t st = smem_u32(rring + s * kRawBytes);
+        const uint32_t fb = smem_u32(&rfull[s]);
+        mbar_arrive_expect_tx_if(leader, fb, kRawBytes);
+        bulk_g2s_if(leader, st, p.wcodes + (blk + ks) * kCodeBytes, kCodeBytes, fb, pol);
+        bulk_g2s_if(leader, st + kCodeBytes, p.wscales + (blk + ks) * kScaleBytes, kScaleBytes, fb,
+                    pol);
       }
-      if (!ok) {  // let the copies already issued land before the CTA can exit
-        const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
-        for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
-      }
+    }
+    if (!ok) {  // let the copies already issued land before the CTA can exit
+      const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
+      for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
     }
   } else if (warp == 14) {
     // ------------------------------------------------------------ pair-row TMA producer
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_last();
-      uint32_t it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int t = u / p.nrb;
-        const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
-        const int nb16 = (rows + 15) >> 4;
-        const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % BS;
-          if (!mbar_wait(smem_u32(&bempty[s]), ((it / BS) & 1) ^ 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = bring + s * C::kBBytes;
-          const uint32_t fb = smem_u32(&bfull[s]);
-          mbar_arrive_expect_tx(fb, tx);
-#pragma unroll
-          for (int sl = 0; sl < 2; ++sl)
-            for (int g = 0; g < nb16; ++g)
-              tma_load_2d(smem_u32(st + sl * C::kBSlab + g * 2048), &tmap_b, ks * kBK + sl * 64,
-                          start + g * 16, fb, pol);
+    const uint32_t leader = elect_one();
+    const uint64_t pol = l2_policy_evict_last();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int t = u / p.nrb;
+      const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
+      const int nb16 = (rows + 15) >> 4;
+      const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int s = it % BS;
+        if (!warp_wait(smem_u32(&bempty[s]), ((it / BS) & 1) ^ 1, abort_flag, p.err)) {
+          ok = false;
+          break;
         }
+        const uint32_t st = smem_u32(bring + s * C::kBBytes);
+        const uint32_t fb = smem_u32(&bfull[s]);
+        mbar_arrive_expect_tx_if(leader, fb, tx);
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+          for (int g = 0; g < nb16; ++g)
+            tma_load_2d_if(leader, st + sl * C::kBSlab + g * 2048, &tmap_b, ks * kBK + sl * 64,
+                           start + g * 16, fb, pol);
       }
-      if (!ok) {
-        const uint32_t first = it > (uint32_t)BS ? it - BS : 0u;
-        for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&bfull[j % BS]), (j / BS) & 1);
-      }
+    }
+    if (!ok) {
+      const uint32_t first = it > (uint32_t)BS ? it - BS : 0u;
+      for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&bfull[j % BS]), (j / BS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, local = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
-        const int t = u / p.nrb;
-        const int rows = p.tiles[3 * t + 2];
-        const uint32_t idesc = idesc_bf16_f32(128, ((rows + 15) >> 4) << 4);
-        const int ab = local % ACCB;
-        if (!mbar_wait(smem_u32(&acce[ab]), ((local / ACCB) & 1) ^ 1, abort_flag, p.err)) {
+    // (whole warp, converged; one elected lane issues every tcgen05.mma / commit)
+    const uint32_t leader = elect_one();
+    uint32_t it = 0, local = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
+      const int t = u / p.nrb;
+      const int rows = p.tiles[3 * t + 2];
+      const uint32_t idesc = idesc_bf16_f32(128, ((rows + 15) >> 4) << 4);
+      const int ab = local % ACCB;
+      if (!warp_wait(smem_u32(&acce[ab]), ((local / ACCB) & 1) ^ 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int a = it % AS, b = it % BS;
+        if (!warp_wait(smem_u32(&bfull[b]), (it / BS) & 1, abort_flag, p.err) ||
+            !warp_wait(smem_u32(&afull[a]), (it / AS) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int a = it % AS, b = it % BS;
-          if (!mbar_wait(smem_u32(&bfull[b]), (it / BS) & 1, abort_flag, p.err) ||
-              !mbar_wait(smem_u32(&afull[a]), (it / AS) & 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t b0 = smem_u32(bring + b * C::kBBytes);
+        // descriptor of the step's first 16-wide K slice; the others differ only in
+        // the start-address field (16-byte units, no carry: smem < 256 KB)
+        const uint64_t bdesc = sdesc_sw128(smem_u32(bring + b * C::kBBytes));
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t baddr = b0 + (j >> 2) * C::kBSlab + (j & 3) * 32;
-            mma_bf16_ts(d_tmem, tmem + a * 64 + j * 8, sdesc_sw128(baddr), idesc,
-                        (ks | j) != 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&aempty[a]));
-          tc_commit(smem_u32(&bempty[b]));
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t off16 = (uint32_t)(((j >> 2) * C::kBSlab + (j & 3) * 32) >> 4);
+          mma_bf16_ts_if(leader, d_tmem, tmem + a * 64 + j * 8, bdesc + off16, idesc,
+                         (ks | j) != 0 ? 1u : 0u);
         }
-        if (ok) tc_commit(smem_u32(&accf[ab]));
+        tc_commit_if(leader, smem_u32(&aempty[a]));
+        tc_commit_if(leader, smem_u32(&bempty[b]));
       }
-      // no MMA may still be running when TMEM is released
-      tc_commit(smem_u32(drain));
-      drain_wait(smem_u32(drain), 0);
+      if (ok) tc_commit_if(leader, smem_u32(&accf[ab]));
     }
+    // no MMA may still be running when TMEM is released
+    tc_commit_if(leader, smem_u32(drain));
+    drain_wait(smem_u32(drain), 0);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ dequant warps 6..13
     const int grp = (warp - 6) >> 2;  // which steps: it % 2 == grp
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < nks; ++ks, ++it) {
         if ((int)(it & 1) != grp) continue;
         const int s = it % RS, a = it % AS;
-        if (!mbar_wait(smem_u32(&rfull[s]), (it / RS) & 1, abort_flag, p.err)) {
+        if (!warp_wait(smem_u32(&rfull[s]), (it / RS) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + row * 8);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw step may be refilled
-        if (!mbar_wait(smem_u32(&aempty[a]), ((it / AS) & 1) ^ 1, abort_flag, p.err)) {
+        if (!warp_wait(smem_u32(&aempty[a]), ((it / AS) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
-      if (!mbar_wait(smem_u32(&accf[ab]), (local / ACCB) & 1, abort_flag, p.err)) break;
+      if (!warp_wait(smem_u32(&accf[ab]), (local / ACCB) & 1, abort_flag, p.err)) break;
       tc_fence_after();
       const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMAX;
@@ -295,27 +296,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_x16(tbase + c0, v);
         tmem_wait_ld();
         if constexpr (FC1) {
-          // lanes 0..15: up rows, lanes 16..31: gate rows of the same 16 indices
+          // lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
+          // intermediate indices.  For each pair of columns (c, c+1) the lanes trade
+          // one value so that lane j < 16 forms h(i, c) and lane j + 16 forms
+          // h(i, c+1): every lane computes and stores.
+          const bool is_up = lane < 16;
           const int i = rb * 64 + q * 16 + (lane & 15);
           __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float mine = __uint_as_float(v[c]) * gsc;
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            if (lane < 16 && c0 + c < rows) {
-              const float gate = other, up = mine;
+          for (int c = 0; c < 16; c += 2) {
+            const float send = __uint_as_float(is_up ? v[c + 1] : v[c]) * gsc;
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float up = is_up ? __uint_as_float(v[c]) * gsc : recv;
+            const float gate = is_up ? recv : __uint_as_float(v[c + 1]) * gsc;
+            const int col = c0 + c + (is_up ? 0 : 1);
+            if (col < rows) {
               const float hv = gate / (1.0f + expf(-gate)) * up;
-              hp[(size_t)(start + c0 + c) * p.I + i] = __float2bfloat16_rn(hv);
+              hp[(size_t)(start + col) * p.I + i] = __float2bfloat16_rn(hv);
             }
           }
         } else {
+          // the chunk's 16 pair ids and routing weights: one coalesced load, then
+          // broadcast by shuffles
+          const int cl = lane & 15;
+          int my_pair = 0;
+          float my_w = 0.f;
+          if (c0 + cl < rows) {
+            my_pair = p.sorted_pair[start + c0 + cl];
+            my_w = p.topk_w[my_pair] * gsc;
+          }
           const int jrow = rb * 128 + q * 32 + lane;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            if (c0 + c < rows) {
-              const int pair = p.sorted_pair[start + c0 + c];
-              p.ypart[(size_t)pair * p.H + jrow] = __uint_as_float(v[c]) * gsc * p.topk_w[pair];
-            }
+            const int pair = __shfl_sync(0xffffffffu, my_pair, c);
+            const float w = __shfl_sync(0xffffffffu, my_w, c);
+            if (c0 + c < rows) p.ypart[(size_t)pair * p.H + jrow] = __uint_as_float(v[c]) * w;
           }
         }
       }
