@@ -40,26 +40,31 @@ constexpr int kScaleBytes = 1024;   // 128 rows x 8 blocks
 constexpr int kRawBytes = kCodeBytes + kScaleBytes;
 constexpr int kTmemCols = 512;
 constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale table
-constexpr int kWarps = 15;          // 0 codes TMA, 1 MMA, 2-5 epilogue, 6-13 dequant, 14 pair-row TMA
-constexpr int kThreads = kWarps * 32;
+// Warp roles: 0 weight TMA, 1 MMA, 2-5 epilogue, 6 pair-row TMA, 7.. dequant (DG groups of 4).
+constexpr int kDequantWarp0 = 7;
+__host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWarp0 + 4 * groups) * 32; }
 
-// Three rings, each with its own depth:
-//   raw ring  (RS stages): packed codes + scales of one 128-wide K step, refilled as
-//             soon as the dequant warps have read it, so many weight bytes stay in
-//             flight per SM (the decode bound is HBM latency x bandwidth);
-//   B ring    (BS stages): the tile's pair rows for one K step, freed by the MMA;
-//   A slots   (AS in TMEM): dequantized bf16 weights, freed by the MMA.
-template <int NMAX, int RS, int BS, int AS, int ACCB>
+// Two rings:
+//   raw ring (RS stages): packed codes + scales of one 128-wide K step, refilled as
+//            soon as the dequant warps have read it, so many weight bytes stay in
+//            flight per SM (the decode bound is HBM latency x bandwidth);
+//   slots    (SL): one K step's operands for the MMA: the dequantized bf16 weights in
+//            a 64-column TMEM slot and the tile's pair rows in an smem stage.  A slot
+//            is "full" when its 4 dequant warps have arrived and the pair rows have
+//            landed, and "empty" when the MMA that read it has completed: one wait
+//            and one commit per step for the MMA warp.
+template <int NMAX, int RS, int SL, int ACCB, int DG>
 struct Cfg {
   static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
   static constexpr int kBBytes = 2 * kBSlab;
-  static constexpr int kAccCol0 = AS * 64;   // TMEM: [A slots: 64 cols each][accumulators]
-  static constexpr int kSmemBytes = BS * kBBytes + RS * kRawBytes + 1024 + kCtrlBytes;
+  static constexpr int kAccCol0 = SL * 64;   // TMEM: [A slots: 64 cols each][accumulators]
+  static constexpr int kSmemBytes = SL * kBBytes + RS * kRawBytes + 1024 + kCtrlBytes;
+  static constexpr int kThreads = gemm_threads(DG);
   static_assert(kBBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte stage alignment");
-  static_assert(AS * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
+  static_assert(SL * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(3 * (RS + BS + AS + ACCB) * 8 + 64 <= 1024, "barrier area");
+  static_assert((2 * (RS + SL + ACCB) + 1) * 8 + 16 <= 1024, "barrier area");
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -70,23 +75,21 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int RS, int BS, int AS, int ACCB, bool FC1>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NMAX, int RS, int SL, int ACCB, int DG, bool FC1>
+__global__ void __launch_bounds__(gemm_threads(DG), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using C = Cfg<NMAX, RS, BS, AS, ACCB>;
+  using C = Cfg<NMAX, RS, SL, ACCB, DG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* bring = smem;                          // [BS][kBBytes]
-  uint8_t* rring = smem + BS * C::kBBytes;        // [RS][kRawBytes]
+  uint8_t* bring = smem;                          // [SL][kBBytes] pair rows
+  uint8_t* rring = smem + SL * C::kBBytes;        // [RS][kRawBytes]
   uint8_t* ctrl = rring + RS * kRawBytes;
   uint64_t* rfull = reinterpret_cast<uint64_t*>(ctrl);  // raw step landed (tx)
   uint64_t* rempty = rfull + RS;                        // raw step read by 4 dequant warps
-  uint64_t* bfull = rempty + RS;                        // pair rows landed (tx)
-  uint64_t* bempty = bfull + BS;                        // pair rows read by the MMA
-  uint64_t* afull = bempty + BS;                        // A slot written by 4 dequant warps
-  uint64_t* aempty = afull + AS;                        // A slot read by the MMA
-  uint64_t* accf = aempty + AS;                         // accumulator ready
+  uint64_t* sfull = rempty + RS;                        // slot: 4 dequant warps + pair rows (tx)
+  uint64_t* sempty = sfull + SL;                        // slot read by the MMA
+  uint64_t* accf = sempty + SL;                         // accumulator ready
   uint64_t* acce = accf + ACCB;                         // accumulator drained (4 warps)
   uint64_t* drain = acce + ACCB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -99,13 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&rfull[s]), 1);
       mbar_init(smem_u32(&rempty[s]), 4);
     }
-    for (int s = 0; s < BS; ++s) {
-      mbar_init(smem_u32(&bfull[s]), 1);
-      mbar_init(smem_u32(&bempty[s]), 1);
-    }
-    for (int s = 0; s < AS; ++s) {
-      mbar_init(smem_u32(&afull[s]), 4);
-      mbar_init(smem_u32(&aempty[s]), 1);
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(smem_u32(&sfull[s]), 5);
+      mbar_init(smem_u32(&sempty[s]), 1);
     }
     for (int a = 0; a < ACCB; ++a) {
       mbar_init(smem_u32(&accf[a]), 1);
@@ -115,12 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int b = threadIdx.x; b < 256; b += kThreads) scale_lut[b] = e4m3_scale_bf16x2(b);
+  for (int b = threadIdx.x; b < 256; b += C::kThreads) scale_lut[b] = e4m3_scale_bf16x2(b);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 14 && lane == 0) prefetch_tmap(&tmap_b);
+  if (warp == 6 && lane == 0) prefetch_tmap(&tmap_b);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -158,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
       for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
     }
-  } else if (warp == 14) {
+  } else if (warp == 6) {
     // ------------------------------------------------------------ pair-row TMA producer
     const uint32_t leader = elect_one();
     const uint64_t pol = l2_policy_evict_last();
@@ -170,13 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nb16 = (rows + 15) >> 4;
       const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int s = it % BS;
-        if (!warp_wait(smem_u32(&bempty[s]), ((it / BS) & 1) ^ 1, abort_flag, p.err)) {
+        const int s = it % SL;
+        if (!warp_wait(smem_u32(&sempty[s]), ((it / SL) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         const uint32_t st = smem_u32(bring + s * C::kBBytes);
-        const uint32_t fb = smem_u32(&bfull[s]);
+        const uint32_t fb = smem_u32(&sfull[s]);
         mbar_arrive_expect_tx_if(leader, fb, tx);
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
@@ -185,9 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                            start + g * 16, fb, pol);
       }
     }
-    if (!ok) {
-      const uint32_t first = it > (uint32_t)BS ? it - BS : 0u;
-      for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&bfull[j % BS]), (j / BS) & 1);
+    if (!ok) {  // the pair rows of the last slots may still be landing
+      const unsigned long long t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -207,41 +207,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int a = it % AS, b = it % BS;
-        if (!warp_wait(smem_u32(&bfull[b]), (it / BS) & 1, abort_flag, p.err) ||
-            !warp_wait(smem_u32(&afull[a]), (it / AS) & 1, abort_flag, p.err)) {
+        const int sl = it % SL;
+        if (!warp_wait(smem_u32(&sfull[sl]), (it / SL) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // descriptor of the step's first 16-wide K slice; the others differ only in
         // the start-address field (16-byte units, no carry: smem < 256 KB)
-        const uint64_t bdesc = sdesc_sw128(smem_u32(bring + b * C::kBBytes));
+        const uint64_t bdesc = sdesc_sw128(smem_u32(bring + sl * C::kBBytes));
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t off16 = (uint32_t)(((j >> 2) * C::kBSlab + (j & 3) * 32) >> 4);
-          mma_bf16_ts_if(leader, d_tmem, tmem + a * 64 + j * 8, bdesc + off16, idesc,
+          mma_bf16_ts_if(leader, d_tmem, tmem + sl * 64 + j * 8, bdesc + off16, idesc,
                          (ks | j) != 0 ? 1u : 0u);
         }
-        tc_commit_if(leader, smem_u32(&aempty[a]));
-        tc_commit_if(leader, smem_u32(&bempty[b]));
+        tc_commit_if(leader, smem_u32(&sempty[sl]));
       }
       if (ok) tc_commit_if(leader, smem_u32(&accf[ab]));
     }
     // no MMA may still be running when TMEM is released
     tc_commit_if(leader, smem_u32(drain));
     drain_wait(smem_u32(drain), 0);
-  } else if (warp >= 6) {
-    // ------------------------------------------------------------ dequant warps 6..13
-    const int grp = (warp - 6) >> 2;  // which steps: it % 2 == grp
+  } else if (warp >= kDequantWarp0) {
+    // ------------------------------------------------------------ dequant warps (DG groups)
+    const int grp = (warp - kDequantWarp0) >> 2;  // which steps: it % DG == grp
     const int q = warp & 3;           // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;    // weight row of the 128-row block
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        if ((int)(it & 1) != grp) continue;
-        const int s = it % RS, a = it % AS;
+        if ((int)(it % DG) != grp) continue;
+        const int s = it % RS, a = it % SL;
         if (!warp_wait(smem_u32(&rfull[s]), (it / RS) & 1, abort_flag, p.err)) {
           ok = false;
           break;
@@ -254,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + row * 8);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw step may be refilled
-        if (!warp_wait(smem_u32(&aempty[a]), ((it / AS) & 1) ^ 1, abort_flag, p.err)) {
+        if (!warp_wait(smem_u32(&sempty[a]), ((it / SL) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -276,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[a]));
+        if (lane == 0) mbar_arrive(smem_u32(&sfull[a]));
       }
     }
   } else {
@@ -348,13 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NMAX, int RS, int BS, int AS, int ACCB, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, bool FC1>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
-  using C = Cfg<NMAX, RS, BS, AS, ACCB>;
-  auto* k = moe_gemm_kernel<NMAX, RS, BS, AS, ACCB, FC1>;
+  using C = Cfg<NMAX, RS, SL, ACCB, DG>;
+  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
-  k<<<num_sms, kThreads, C::kSmemBytes, stream>>>(tmap, p);
+  k<<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(tmap, p);
   return cudaGetLastError();
 }
 
@@ -362,18 +360,18 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 
 int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 256; }
 
-// decode : tiles <= 32 pairs, 14 weight steps in flight (126 KB), 8 pair-row steps,
-//          6 TMEM A slots, 2 accumulators
-// prefill: tiles <= 256 pairs, 8 weight steps, 2 pair-row steps (64 KB each),
-//          3 TMEM A slots, 1 accumulator (256 columns)
+// decode : tiles <= 32 pairs, 14 weight steps in flight (126 KB), 6 slots, 2 accumulators,
+//          3 dequant groups
+// prefill: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair rows each),
+//          1 accumulator (256 columns), 2 dequant groups
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
   if (sched == QMOE_SCHED_DECODE)
-    return fc1 ? run<32, 14, 8, 6, 2, true>(tmap_b, p, num_sms, stream)
-               : run<32, 14, 8, 6, 2, false>(tmap_b, p, num_sms, stream);
-  return fc1 ? run<256, 8, 2, 3, 1, true>(tmap_b, p, num_sms, stream)
-             : run<256, 8, 2, 3, 1, false>(tmap_b, p, num_sms, stream);
+    return fc1 ? run<32, 14, 6, 2, 3, true>(tmap_b, p, num_sms, stream)
+               : run<32, 14, 6, 2, 3, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<256, 8, 2, 1, 2, true>(tmap_b, p, num_sms, stream)
+             : run<256, 8, 2, 1, 2, false>(tmap_b, p, num_sms, stream);
 }
 
 }  // namespace qmoe
