@@ -51,6 +51,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while the
+// phase is incomplete (the thread resumes as soon as it completes): waiting warps
+// sleep instead of spinning through issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -67,8 +81,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
+    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+    if ((i & 3) == 0) {
       if (*abort_flag) return false;
       if ((long long)(globaltimer_ns() - t0) > limit_ns) {
         *abort_flag = 1;
@@ -208,6 +222,42 @@ __device__ __forceinline__ void mma_bf16_ts_if(uint32_t pred, uint32_t d_tmem, u
       "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The 8 MMAs of one 128-wide K step in one block, issued by the elected lane:
+// D (+)= A[a_tmem + 8j] * B[desc + 2j] for j = 0..7 (16-wide K slices; the B slices
+// 2..3 and 4..7 sit in a second 64-wide slab `slab16` 16-byte units further on).
+// Only the first MMA can start a fresh accumulation.  Keeping the issue to about
+// three instructions per MMA matters: the issuing warp shares its scheduler with
+// dequant warps, and the MMA pipe runs dry while it executes anything else.
+__device__ __forceinline__ void mma_bf16_ts_step8(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint32_t desc_lo, uint32_t desc_hi,
+                                                  uint32_t slab16, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, t;\n\t.reg .b64 d;\n\t.reg .b32 lo, a;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "setp.ne.b32 q, %7, 0;\n\t"
+      "setp.eq.u32 t, 0, 0;\n\t"
+      "mov.b64 d, {%3, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], d, %6, q;\n\t"
+      "add.u32 lo, %3, 2;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 8;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t"
+      "add.u32 lo, %3, 4;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 16;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t"
+      "add.u32 lo, %3, 6;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 24;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t"
+      "add.u32 lo, %3, %5;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 32;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t"
+      "add.u32 lo, lo, 2;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 40;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t"
+      "add.u32 lo, lo, 2;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 48;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t"
+      "add.u32 lo, lo, 2;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 56;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %6, t;\n\t}" ::"r"(pred),
+      "r"(d_tmem), "r"(a_tmem), "r"(desc_lo), "r"(desc_hi), "r"(slab16), "r"(idesc),
+      "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (bf16 inputs, fp32 accumulate).
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {

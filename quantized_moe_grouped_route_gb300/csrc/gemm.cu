@@ -194,6 +194,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // (whole warp, converged; one elected lane issues every tcgen05.mma / commit)
     const uint32_t leader = elect_one();
     uint32_t it = 0, local = 0;
+    // slot index and phase kept incrementally; descriptor of slot 0's first K slice
+    int sl = 0;
+    uint32_t sph = 0;
+    const uint32_t sfull_u = smem_u32(&sfull[0]), sempty_u = smem_u32(&sempty[0]);
+    const uint64_t bdesc0 = sdesc_sw128(smem_u32(bring));
+    const uint32_t bdesc_lo0 = (uint32_t)bdesc0, bdesc_hi = (uint32_t)(bdesc0 >> 32);
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
       const int t = u / p.nrb;
@@ -207,22 +213,18 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int sl = it % SL;
-        if (!warp_wait(smem_u32(&sfull[sl]), (it / SL) & 1, abort_flag, p.err)) {
+        if (!warp_wait(sfull_u + sl * 8, sph, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // descriptor of the step's first 16-wide K slice; the others differ only in
-        // the start-address field (16-byte units, no carry: smem < 256 KB)
-        const uint64_t bdesc = sdesc_sw128(smem_u32(bring + sl * C::kBBytes));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t off16 = (uint32_t)(((j >> 2) * C::kBSlab + (j & 3) * 32) >> 4);
-          mma_bf16_ts_if(leader, d_tmem, tmem + sl * 64 + j * 8, bdesc + off16, idesc,
-                         (ks | j) != 0 ? 1u : 0u);
+        mma_bf16_ts_step8(leader, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (C::kBBytes >> 4),
+                          bdesc_hi, C::kBSlab >> 4, idesc, ks != 0 ? 1u : 0u);
+        tc_commit_if(leader, sempty_u + sl * 8);
+        if (++sl == SL) {
+          sl = 0;
+          sph ^= 1u;
         }
-        tc_commit_if(leader, smem_u32(&sempty[sl]));
       }
       if (ok) tc_commit_if(leader, smem_u32(&accf[ab]));
     }
