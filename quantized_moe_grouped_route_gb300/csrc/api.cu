@@ -45,16 +45,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 [rows][cols] operand, boxes of 64 columns x 16 rows, 128-byte swizzle.
-int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols) {
+// Tensor map over a row-major bf16 matrix [rows][cols] for the GEMM's pair rows.
+// box_rows == 0: 2-D, box 16 rows x 64 elements.  box_rows > 0: 3-D view
+// {64 elements, rows, cols / 64 slabs} (slab stride 128 bytes), box {64, box_rows, 2},
+// which lands in shared memory as [slab][row][64 elements].
+int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return QMOE_ERR_CUDA;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (box_rows == 0) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)cols / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? QMOE_OK : QMOE_ERR_CUDA;
 }
 
@@ -230,8 +245,9 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   float* ypart = reinterpret_cast<float*>(ws + L.ypart);
 
   CUtensorMap map_x, map_h;
-  if (make_tmap_rows(&map_x, xs, L.rows, H) != QMOE_OK) return QMOE_ERR_CUDA;
-  if (make_tmap_rows(&map_h, h, L.rows, I) != QMOE_OK) return QMOE_ERR_CUDA;
+  const int box_rows = gemm_b_box_rows(rsched);
+  if (make_tmap_rows(&map_x, xs, L.rows, H, box_rows) != QMOE_OK) return QMOE_ERR_CUDA;
+  if (make_tmap_rows(&map_h, h, L.rows, I, box_rows) != QMOE_OK) return QMOE_ERR_CUDA;
 
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;

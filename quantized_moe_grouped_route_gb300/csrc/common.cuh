@@ -164,6 +164,18 @@ __device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, cons
       : "memory");
 }
 
+// 3-D tiled tensor copy by one lane (pred != 0); x (innermost) must be a multiple of
+// 8 bf16 elements.
+__device__ __forceinline__ void tma_load_3d_if(uint32_t pred, uint32_t dst, const CUtensorMap* map,
+                                               int x, int y, int z, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%1], [%2, {%3, %4, %5}], [%6], %7;\n\t}" ::"r"(pred),
+      "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled tensor copy; x (innermost) must be a multiple of 8 bf16 elements.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar, uint64_t policy) {

@@ -17,7 +17,7 @@
 //                   swizzle) into the pair-row ring
 //   dequant warps : codes -> bf16 in registers (bit placement + one bf16x2 multiply
 //                   by the block scale) -> tcgen05.st into TMEM (the MMA's A operand)
-//   MMA thread    : 8 x tcgen05.mma kind::f16, A from TMEM, B from smem, fp32
+//   MMA warp      : 8 x tcgen05.mma kind::f16, A from TMEM, B from smem, fp32
 //                   accumulator in TMEM; commits release the stage
 //   epilogue warps: tcgen05.ld of the accumulator, scale, SwiGLU or routing weight,
 //                   global stores
@@ -40,7 +40,16 @@ constexpr int kScaleBytes = 1024;   // 128 rows x 8 blocks
 constexpr int kRawBytes = kCodeBytes + kScaleBytes;
 constexpr int kTmemCols = 512;
 constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale table
-// Warp roles: 0 weight TMA, 1 MMA, 2-5 epilogue, 6 pair-row TMA, 7.. dequant (DG groups of 4).
+
+// Warp roles: 0 MMA issue, 1 pair-row TMA, 2 weight TMA, 3..6 epilogue (one per TMEM
+// lane quarter), 7.. dequant (DG groups of 4 warps).  Warp w runs on scheduler w % 4
+// and may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so every group of four
+// consecutive warps covers the 128 lanes once, and the three latency-critical issuers
+// (MMA, pair rows, weights) sit on three different schedulers.
+constexpr int kMmaWarp = 0;
+constexpr int kPairTmaWarp = 1;
+constexpr int kWeightTmaWarp = 2;
+constexpr int kEpiWarp0 = 3;
 constexpr int kDequantWarp0 = 7;
 __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWarp0 + 4 * groups) * 32; }
 
@@ -51,18 +60,31 @@ __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWar
 //   slots    (SL): one K step's operands for the MMA: the dequantized bf16 weights in
 //            a 64-column TMEM slot and the tile's pair rows in an smem stage.  A slot
 //            is "full" when its 4 dequant warps have arrived and the pair rows have
-//            landed, and "empty" when the MMA that read it has completed: one wait
-//            and one commit per step for the MMA warp.
+//            landed, and "empty" when the MMAs that read it have completed.
+// Barrier waits use phase parity, which cannot tell phase k from phase k+2.  Every
+// slot must therefore be filled and drained by single ordered streams: all uses of a
+// slot (steps s, s+SL, s+2SL, ..) go to the same dequant group, i.e. SL is a multiple
+// of DG, and likewise RS for the weight ring.  Otherwise a warp that runs a full ring
+// cycle ahead of asynchronous completions (which may land out of order) can pass a
+// wait early, and the rings desynchronise (checked by simulating the protocol).
+//
+// Pair rows: with B3D the tile's rows of one K step (both 64-wide slabs) arrive in a
+// single 3-D box copy {64 elements, NMAX rows, 2 slabs}; otherwise as 2-D boxes of 16
+// rows x 64 elements, as many as the tile needs.  The copy instruction is issued from
+// one warp that also serves every step's barrier traffic, so fewer copies per step
+// shorten the loop that feeds the MMA.
 template <int NMAX, int RS, int SL, int ACCB, int DG>
 struct Cfg {
   static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
   static constexpr int kBBytes = 2 * kBSlab;
-  static constexpr int kAccCol0 = SL * 64;   // TMEM: [A slots: 64 cols each][accumulators]
+  static constexpr int kAccCol0 = SL * 64;   // TMEM: [A slots: 64 cols][acc: ACCB x NMAX]
   static constexpr int kSmemBytes = SL * kBBytes + RS * kRawBytes + 1024 + kCtrlBytes;
   static constexpr int kThreads = gemm_threads(DG);
   static_assert(kBBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte stage alignment");
   static_assert(SL * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
+  static_assert(SL % DG == 0, "each slot needs one dequant group");
+  static_assert(RS % DG == 0, "each weight stage needs one dequant group");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert((2 * (RS + SL + ACCB) + 1) * 8 + 16 <= 1024, "barrier area");
 };
@@ -75,7 +97,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, bool B3D, bool FC1>
 __global__ void __launch_bounds__(gemm_threads(DG), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG>;
@@ -88,9 +110,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   uint64_t* rfull = reinterpret_cast<uint64_t*>(ctrl);  // raw step landed (tx)
   uint64_t* rempty = rfull + RS;                        // raw step read by 4 dequant warps
   uint64_t* sfull = rempty + RS;                        // slot: 4 dequant warps + pair rows (tx)
-  uint64_t* sempty = sfull + SL;                        // slot read by the MMA
-  uint64_t* accf = sempty + SL;                         // accumulator ready
-  uint64_t* acce = accf + ACCB;                         // accumulator drained (4 warps)
+  uint64_t* sempty = sfull + SL;                        // slot read by the MMAs
+  uint64_t* accf = sempty + SL;                         // accumulator ready (MMA commit)
+  uint64_t* acce = accf + ACCB;                         // accumulators drained (4 warps)
   uint64_t* drain = acce + ACCB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -115,11 +137,11 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     fence_mbar_init();
   }
   for (int b = threadIdx.x; b < 256; b += C::kThreads) scale_lut[b] = e4m3_scale_bf16x2(b);
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 6 && lane == 0) prefetch_tmap(&tmap_b);
+  if (warp == kPairTmaWarp && lane == 0) prefetch_tmap(&tmap_b);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -128,7 +150,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   const int nks = p.K / kBK;
   const int n_units = (*p.n_tiles) * p.nrb;
 
-  if (warp == 0) {
+  if (warp == kWeightTmaWarp) {
     // ------------------------------------------------------------ weight TMA producer
     // (whole warp, converged; one elected lane issues)
     const uint32_t leader = elect_one();
@@ -157,7 +179,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
       for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
     }
-  } else if (warp == 6) {
+  } else if (warp == kPairTmaWarp) {
     // ------------------------------------------------------------ pair-row TMA producer
     const uint32_t leader = elect_one();
     const uint64_t pol = l2_policy_evict_last();
@@ -166,7 +188,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int t = u / p.nrb;
       const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
-      const int nb16 = (rows + 15) >> 4;
+      const int nb16 = B3D ? NMAX / 16 : (rows + 15) >> 4;
       const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
       for (int ks = 0; ks < nks; ++ks, ++it) {
         const int s = it % SL;
@@ -177,11 +199,15 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         const uint32_t st = smem_u32(bring + s * C::kBBytes);
         const uint32_t fb = smem_u32(&sfull[s]);
         mbar_arrive_expect_tx_if(leader, fb, tx);
+        if constexpr (B3D) {
+          tma_load_3d_if(leader, st, &tmap_b, 0, start, 2 * ks, fb, pol);
+        } else {
 #pragma unroll
-        for (int sl = 0; sl < 2; ++sl)
-          for (int g = 0; g < nb16; ++g)
-            tma_load_2d_if(leader, st + sl * C::kBSlab + g * 2048, &tmap_b, ks * kBK + sl * 64,
-                           start + g * 16, fb, pol);
+          for (int sl = 0; sl < 2; ++sl)
+            for (int g = 0; g < nb16; ++g)
+              tma_load_2d_if(leader, st + sl * C::kBSlab + g * 2048, &tmap_b, ks * kBK + sl * 64,
+                             start + g * 16, fb, pol);
+        }
       }
     }
     if (!ok) {  // the pair rows of the last slots may still be landing
@@ -189,17 +215,14 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       while (globaltimer_ns() - t0 < 2000000ull) {
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // (whole warp, converged; one elected lane issues every tcgen05.mma / commit)
+    // Whole warp, converged; one elected lane issues.
     const uint32_t leader = elect_one();
-    uint32_t it = 0, local = 0;
-    // slot index and phase kept incrementally; descriptor of slot 0's first K slice
-    int sl = 0;
-    uint32_t sph = 0;
     const uint32_t sfull_u = smem_u32(&sfull[0]), sempty_u = smem_u32(&sempty[0]);
     const uint64_t bdesc0 = sdesc_sw128(smem_u32(bring));
     const uint32_t bdesc_lo0 = (uint32_t)bdesc0, bdesc_hi = (uint32_t)(bdesc0 >> 32);
+    uint32_t it = 0, local = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
       const int t = u / p.nrb;
@@ -212,8 +235,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        if (!warp_wait(sfull_u + sl * 8, sph, abort_flag, p.err)) {
+      for (int ks = 0; ks < nks; ++ks) {
+        const uint32_t sit = it + (uint32_t)ks;
+        const int sl = sit % SL;
+        if (!warp_wait(sfull_u + sl * 8, (sit / SL) & 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -221,11 +246,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         mma_bf16_ts_step8(leader, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (C::kBBytes >> 4),
                           bdesc_hi, C::kBSlab >> 4, idesc, ks != 0 ? 1u : 0u);
         tc_commit_if(leader, sempty_u + sl * 8);
-        if (++sl == SL) {
-          sl = 0;
-          sph ^= 1u;
-        }
       }
+      it += nks;
       if (ok) tc_commit_if(leader, smem_u32(&accf[ab]));
     }
     // no MMA may still be running when TMEM is released
@@ -234,8 +256,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant warps (DG groups)
     const int grp = (warp - kDequantWarp0) >> 2;  // which steps: it % DG == grp
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;    // weight row of the 128-row block
+    const int q = warp & 3;                       // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;                // weight row of the 128-row block
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -279,8 +301,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         if (lane == 0) mbar_arrive(smem_u32(&sfull[a]));
       }
     }
-  } else {
-    // ------------------------------------------------------------ epilogue warps 2..5
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+    // ------------------------------------------------------------ epilogue warps 4..7
     const int q = warp & 3;
     uint32_t local = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
@@ -292,9 +314,14 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMAX;
       for (int c0 = 0; c0 < rows; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(tbase + c0, v);
-        tmem_wait_ld();
+        float v[16];
+        {
+          uint32_t r[16];
+          tmem_ld_x16(tbase + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
+        }
         if constexpr (FC1) {
           // lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
           // intermediate indices.  For each pair of columns (c, c+1) the lanes trade
@@ -305,10 +332,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
 #pragma unroll
           for (int c = 0; c < 16; c += 2) {
-            const float send = __uint_as_float(is_up ? v[c + 1] : v[c]) * gsc;
+            const float send = (is_up ? v[c + 1] : v[c]) * gsc;
             const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float up = is_up ? __uint_as_float(v[c]) * gsc : recv;
-            const float gate = is_up ? recv : __uint_as_float(v[c + 1]) * gsc;
+            const float up = is_up ? v[c] * gsc : recv;
+            const float gate = is_up ? recv : v[c + 1] * gsc;
             const int col = c0 + c + (is_up ? 0 : 1);
             if (col < rows) {
               const float hv = gate / (1.0f + expf(-gate)) * up;
@@ -330,7 +357,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           for (int c = 0; c < 16; ++c) {
             const int pair = __shfl_sync(0xffffffffu, my_pair, c);
             const float w = __shfl_sync(0xffffffffu, my_w, c);
-            if (c0 + c < rows) p.ypart[(size_t)pair * p.H + jrow] = __uint_as_float(v[c]) * w;
+            if (c0 + c < rows) p.ypart[(size_t)pair * p.H + jrow] = v[c] * w;
           }
         }
       }
@@ -342,16 +369,16 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, bool B3D, bool FC1>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG>;
-  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, FC1>;
+  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, B3D, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   k<<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(tmap, p);
@@ -362,18 +389,20 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 
 int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 256; }
 
-// decode : tiles <= 32 pairs, 14 weight steps in flight (126 KB), 6 slots, 2 accumulators,
-//          3 dequant groups
+int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 0; }
+
+// decode : tiles <= 32 pairs, 15 weight steps in flight (135 KB), 6 slots, 2 accumulator
+//          buffers, 3 dequant groups, pair rows as one 3-D box per step
 // prefill: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair rows each),
-//          1 accumulator (256 columns), 2 dequant groups
+//          1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 16 rows
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
   if (sched == QMOE_SCHED_DECODE)
-    return fc1 ? run<32, 14, 6, 2, 3, true>(tmap_b, p, num_sms, stream)
-               : run<32, 14, 6, 2, 3, false>(tmap_b, p, num_sms, stream);
-  return fc1 ? run<256, 8, 2, 1, 2, true>(tmap_b, p, num_sms, stream)
-             : run<256, 8, 2, 1, 2, false>(tmap_b, p, num_sms, stream);
+    return fc1 ? run<32, 15, 6, 2, 3, true, true>(tmap_b, p, num_sms, stream)
+               : run<32, 15, 6, 2, 3, true, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<256, 8, 2, 1, 2, false, true>(tmap_b, p, num_sms, stream)
+             : run<256, 8, 2, 1, 2, false, false>(tmap_b, p, num_sms, stream);
 }
 
 }  // namespace qmoe
