@@ -255,51 +255,51 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     drain_wait(smem_u32(drain), 0);
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant warps (DG groups)
-    const int grp = (warp - kDequantWarp0) >> 2;  // which steps: it % DG == grp
+    const int grp = (warp - kDequantWarp0) >> 2;  // this group's steps: grp, grp + DG, ..
     const int q = warp & 3;                       // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;                // weight row of the 128-row block
-    uint32_t it = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        if ((int)(it % DG) != grp) continue;
-        const int s = it % RS, a = it % SL;
-        if (!warp_wait(smem_u32(&rfull[s]), (it / RS) & 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* st = rring + s * kRawBytes;
-        const uint4* codes = reinterpret_cast<const uint4*>(st);
-        uint4 cw[4];
+    // The dequant warps only walk the CTA's step sequence: units u = blockIdx.x,
+    // blockIdx.x + gridDim.x, .. of nks steps each.  RS and SL are multiples of DG, so
+    // the group meets the same ring residues on every lap (s, a) and the phase bits
+    // flip on each wrap.
+    const int my_units = blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const uint32_t total = (uint32_t)my_units * (uint32_t)nks;
+    uint32_t s = grp, a = grp, rph = 0, aph = 0;
+    for (uint32_t it = grp; it < total; it += DG) {
+      if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;
+      const uint8_t* st = rring + s * kRawBytes;
+      const uint4* codes = reinterpret_cast<const uint4*>(st);
+      uint4 cw[4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) cw[kk] = codes[kk * 128 + row];
-        const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + row * 8);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw step may be refilled
-        if (!warp_wait(smem_u32(&sempty[a]), ((it / SL) & 1) ^ 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * 64;
+      for (int kk = 0; kk < 4; ++kk) cw[kk] = codes[kk * 128 + row];
+      const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + row * 8);
+      // the row's 8 block scales as bf16x2 multipliers, all looked up before the first
+      // TMEM store (whose ordering constraint would otherwise serialize the lookups)
+      uint32_t sv[8];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t sb = (kk < 2) ? sc.x : sc.y;
-          const int sh = 16 * (kk & 1);
-          const uint32_t s0 = scale_lut[(sb >> sh) & 0xFF];
-          const uint32_t s1 = scale_lut[(sb >> (sh + 8)) & 0xFF];
-          uint32_t o[16];
-          dequant8(cw[kk].x, s0, o + 0);
-          dequant8(cw[kk].y, s0, o + 4);
-          dequant8(cw[kk].z, s1, o + 8);
-          dequant8(cw[kk].w, s1, o + 12);
-          tmem_st_x16(ta + kk * 16, o);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sfull[a]));
+      for (int j = 0; j < 8; ++j) sv[j] = scale_lut[((j < 4 ? sc.x : sc.y) >> (8 * (j & 3))) & 0xFF];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw step may be refilled
+      if (!warp_wait(smem_u32(&sempty[a]), aph ^ 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * 64;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t o[16];
+        dequant8(cw[kk].x, sv[2 * kk], o + 0);
+        dequant8(cw[kk].y, sv[2 * kk], o + 4);
+        dequant8(cw[kk].z, sv[2 * kk + 1], o + 8);
+        dequant8(cw[kk].w, sv[2 * kk + 1], o + 12);
+        tmem_st_x16(ta + kk * 16, o);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sfull[a]));
+      s += DG;
+      if (s >= (uint32_t)RS) { s -= RS; rph ^= 1; }
+      a += DG;
+      if (a >= (uint32_t)SL) { a -= SL; aph ^= 1; }
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ------------------------------------------------------------ epilogue warps 4..7
