@@ -49,7 +49,7 @@ extern "C" {
 
 /* Tile schedules for moe_nvfp4_forward. */
 #define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
-#define QMOE_SCHED_DECODE 1  /* tiles of <= 32 pairs: weight streaming, HBM bound */
+#define QMOE_SCHED_DECODE 1  /* tiles of <= 16 pairs: weight streaming, HBM bound */
 #define QMOE_SCHED_PREFILL 2 /* tiles of <= 256 pairs: tensor bound */
 
 /* Weight roles for moe_nvfp4_repack. */

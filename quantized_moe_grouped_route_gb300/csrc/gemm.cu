@@ -41,16 +41,18 @@ constexpr int kRawBytes = kCodeBytes + kScaleBytes;
 constexpr int kTmemCols = 512;
 constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale table
 
-// Warp roles: 0 MMA issue, 1 pair-row TMA, 2 weight TMA, 3..6 epilogue (one per TMEM
-// lane quarter), 7.. dequant (DG groups of 4 warps).  Warp w runs on scheduler w % 4
-// and may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so every group of four
-// consecutive warps covers the 128 lanes once, and the three latency-critical issuers
-// (MMA, pair rows, weights) sit on three different schedulers.
-constexpr int kMmaWarp = 0;
-constexpr int kPairTmaWarp = 1;
-constexpr int kWeightTmaWarp = 2;
-constexpr int kEpiWarp0 = 3;
-constexpr int kDequantWarp0 = 7;
+// Warp roles: 0 pair-row TMA, 1..NMW MMA issue (NMW <= 3), 4 weight TMA, 5..8 epilogue
+// (one per TMEM lane quarter), 9.. dequant (DG groups of 4 warps).  Warp w runs on
+// scheduler w % 4 and may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so every
+// group of four consecutive warps covers the 128 lanes once.  Each scheduler carries
+// one dequant warp per group; the MMA issue (eight tcgen05.mma per K step, costly to
+// issue next to busy dequant warps) is spread over schedulers 1..3 and the two TMA
+// producers share scheduler 0.
+constexpr int kPairTmaWarp = 0;
+constexpr int kMmaWarp0 = 1;
+constexpr int kWeightTmaWarp = 4;
+constexpr int kEpiWarp0 = 5;
+constexpr int kDequantWarp0 = 9;
 __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWarp0 + 4 * groups) * 32; }
 
 // Two rings:
@@ -61,29 +63,34 @@ __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWar
 //            a 64-column TMEM slot and the tile's pair rows in an smem stage.  A slot
 //            is "full" when its 4 dequant warps have arrived and the pair rows have
 //            landed, and "empty" when the MMAs that read it have completed.
+// MMA issue: NMW warps take the K steps round robin by global step index, each into
+// its own accumulator; the epilogue adds the accumulators in a fixed order, so the
+// result does not depend on timing.
 // Barrier waits use phase parity, which cannot tell phase k from phase k+2.  Every
 // slot must therefore be filled and drained by single ordered streams: all uses of a
-// slot (steps s, s+SL, s+2SL, ..) go to the same dequant group, i.e. SL is a multiple
-// of DG, and likewise RS for the weight ring.  Otherwise a warp that runs a full ring
-// cycle ahead of asynchronous completions (which may land out of order) can pass a
-// wait early, and the rings desynchronise (checked by simulating the protocol).
+// slot (steps s, s+SL, s+2SL, ..) go to the same dequant group and the same MMA warp,
+// i.e. SL is a multiple of DG and of NMW, and likewise RS of DG for the weight ring.
+// Otherwise a warp that runs a full ring cycle ahead of asynchronous completions
+// (which may land out of order) can pass a wait early, and the rings desynchronise
+// (checked by simulating the protocol).
 //
 // Pair rows: with B3D the tile's rows of one K step (both 64-wide slabs) arrive in a
 // single 3-D box copy {64 elements, NMAX rows, 2 slabs}; otherwise as 2-D boxes of 16
 // rows x 64 elements, as many as the tile needs.  The copy instruction is issued from
 // one warp that also serves every step's barrier traffic, so fewer copies per step
 // shorten the loop that feeds the MMA.
-template <int NMAX, int RS, int SL, int ACCB, int DG>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW>
 struct Cfg {
   static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
   static constexpr int kBBytes = 2 * kBSlab;
-  static constexpr int kAccCol0 = SL * 64;   // TMEM: [A slots: 64 cols][acc: ACCB x NMAX]
+  static constexpr int kAccCol0 = SL * 64;   // TMEM: [A slots: 64 cols][acc: ACCB x NMW x NMAX]
   static constexpr int kSmemBytes = SL * kBBytes + RS * kRawBytes + 1024 + kCtrlBytes;
   static constexpr int kThreads = gemm_threads(DG);
   static_assert(kBBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte stage alignment");
-  static_assert(SL * 64 + ACCB * NMAX <= kTmemCols, "TMEM budget");
+  static_assert(SL * 64 + ACCB * NMW * NMAX <= kTmemCols, "TMEM budget");
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
-  static_assert(SL % DG == 0, "each slot needs one dequant group");
+  static_assert(NMW >= 1 && NMW <= 3, "MMA warps 1..3");
+  static_assert(SL % DG == 0 && SL % NMW == 0, "each slot needs one dequant group and one MMA warp");
   static_assert(RS % DG == 0, "each weight stage needs one dequant group");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert((2 * (RS + SL + ACCB) + 1) * 8 + 16 <= 1024, "barrier area");
@@ -97,10 +104,10 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, bool B3D, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool B3D, bool FC1>
 __global__ void __launch_bounds__(gemm_threads(DG), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using C = Cfg<NMAX, RS, SL, ACCB, DG>;
+  using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -111,7 +118,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   uint64_t* rempty = rfull + RS;                        // raw step read by 4 dequant warps
   uint64_t* sfull = rempty + RS;                        // slot: 4 dequant warps + pair rows (tx)
   uint64_t* sempty = sfull + SL;                        // slot read by the MMAs
-  uint64_t* accf = sempty + SL;                         // accumulator ready (MMA commit)
+  uint64_t* accf = sempty + SL;                         // accumulators ready (NMW commits)
   uint64_t* acce = accf + ACCB;                         // accumulators drained (4 warps)
   uint64_t* drain = acce + ACCB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -129,15 +136,15 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       mbar_init(smem_u32(&sempty[s]), 1);
     }
     for (int a = 0; a < ACCB; ++a) {
-      mbar_init(smem_u32(&accf[a]), 1);
+      mbar_init(smem_u32(&accf[a]), NMW);
       mbar_init(smem_u32(&acce[a]), 4);
     }
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(drain), NMW);
     *abort_flag = 0;
     fence_mbar_init();
   }
   for (int b = threadIdx.x; b < 256; b += C::kThreads) scale_lut[b] = e4m3_scale_bf16x2(b);
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -215,9 +222,11 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       while (globaltimer_ns() - t0 < 2000000ull) {
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + NMW) {
+    // ------------------------------------------------------------ MMA issuers
+    // MMA warp m takes the global K steps g with g % NMW == m, into its own accumulator.
     // Whole warp, converged; one elected lane issues.
+    const int m = warp - kMmaWarp0;
     const uint32_t leader = elect_one();
     const uint32_t sfull_u = smem_u32(&sfull[0]), sempty_u = smem_u32(&sempty[0]);
     const uint64_t bdesc0 = sdesc_sw128(smem_u32(bring));
@@ -234,8 +243,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + C::kAccCol0 + ab * NMAX;
-      for (int ks = 0; ks < nks; ++ks) {
+      const uint32_t d_tmem = tmem + C::kAccCol0 + (ab * NMW + m) * NMAX;
+      // this warp's first step of the unit: global step it + ks with (it + ks) % NMW == m
+      const int ks0 = (m - (int)(it % NMW) + NMW) % NMW;
+      for (int ks = ks0; ks < nks; ks += NMW) {
         const uint32_t sit = it + (uint32_t)ks;
         const int sl = sit % SL;
         if (!warp_wait(sfull_u + sl * 8, (sit / SL) & 1, abort_flag, p.err)) {
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         }
         tc_fence_after();
         mma_bf16_ts_step8(leader, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (C::kBBytes >> 4),
-                          bdesc_hi, C::kBSlab >> 4, idesc, ks != 0 ? 1u : 0u);
+                          bdesc_hi, C::kBSlab >> 4, idesc, ks != ks0 ? 1u : 0u);
         tc_commit_if(leader, sempty_u + sl * 8);
       }
       it += nks;
@@ -302,25 +313,31 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       if (a >= (uint32_t)SL) { a -= SL; aph ^= 1; }
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
-    // ------------------------------------------------------------ epilogue warps 4..7
+    // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;
-    uint32_t local = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local) {
+    uint32_t local = 0, it0 = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local, it0 += nks) {
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
       if (!warp_wait(smem_u32(&accf[ab]), (local / ACCB) & 1, abort_flag, p.err)) break;
       tc_fence_after();
       const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMAX;
+      const uint32_t tbase =
+          tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMW * NMAX;
       for (int c0 = 0; c0 < rows; c0 += 16) {
         float v[16];
-        {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = 0.f;
+        // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this unit
+        // iff its first step ks0 = (m - it0 % NMW) mod NMW lies inside the unit
+        for (int m = 0; m < NMW; ++m) {
+          if ((m - (int)(it0 % NMW) + NMW) % NMW >= nks) continue;
           uint32_t r[16];
-          tmem_ld_x16(tbase + c0, r);
+          tmem_ld_x16(tbase + m * NMAX + c0, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
         }
         if constexpr (FC1) {
           // lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
@@ -369,16 +386,16 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, bool B3D, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool B3D, bool FC1>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
-  using C = Cfg<NMAX, RS, SL, ACCB, DG>;
-  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, B3D, FC1>;
+  using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW>;
+  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, B3D, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   k<<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(tmap, p);
@@ -387,22 +404,22 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 
 }  // namespace
 
-int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 256; }
+int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 256; }
 
-int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 32 : 0; }
+int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 0; }
 
-// decode : tiles <= 32 pairs, 15 weight steps in flight (135 KB), 6 slots, 2 accumulator
-//          buffers, 3 dequant groups, pair rows as one 3-D box per step
+// decode : tiles <= 16 pairs, 15 weight steps in flight (135 KB), 6 slots, 3 MMA warps
+//          x 2 accumulator buffers, 3 dequant groups, pair rows as one 3-D box per step
 // prefill: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair rows each),
-//          1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 16 rows
+//          1 MMA warp, 1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 16 rows
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
   if (sched == QMOE_SCHED_DECODE)
-    return fc1 ? run<32, 15, 6, 2, 3, true, true>(tmap_b, p, num_sms, stream)
-               : run<32, 15, 6, 2, 3, true, false>(tmap_b, p, num_sms, stream);
-  return fc1 ? run<256, 8, 2, 1, 2, false, true>(tmap_b, p, num_sms, stream)
-             : run<256, 8, 2, 1, 2, false, false>(tmap_b, p, num_sms, stream);
+    return fc1 ? run<16, 15, 6, 2, 3, 3, true, true>(tmap_b, p, num_sms, stream)
+               : run<16, 15, 6, 2, 3, 3, true, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<256, 8, 2, 1, 2, 1, false, true>(tmap_b, p, num_sms, stream)
+             : run<256, 8, 2, 1, 2, 1, false, false>(tmap_b, p, num_sms, stream);
 }
 
 }  // namespace qmoe
