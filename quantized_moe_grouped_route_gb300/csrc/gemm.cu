@@ -41,18 +41,20 @@ constexpr int kRawBytes = kCodeBytes + kScaleBytes;
 constexpr int kTmemCols = 512;
 constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale table
 
-// Warp roles: 0 pair-row TMA, 1..NMW MMA issue (NMW <= 3), 4 weight TMA, 5..8 epilogue
-// (one per TMEM lane quarter), 9.. dequant (DG groups of 4 warps).  Warp w runs on
-// scheduler w % 4 and may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so every
-// group of four consecutive warps covers the 128 lanes once.  Each scheduler carries
-// one dequant warp per group; the MMA issue (eight tcgen05.mma per K step, costly to
-// issue next to busy dequant warps) is spread over schedulers 1..3 and the two TMA
-// producers share scheduler 0.
-constexpr int kPairTmaWarp = 0;
+// Warp roles: 1..NMW MMA issue (NMW <= 3), 4..7 epilogue (one per TMEM lane quarter),
+// 8.. dequant (DG groups of 4 warps); with BIN the MMA warps also issue the pair-row
+// copies of their own steps and warp 0 is the weight TMA producer, otherwise warp 0
+// is a pair-row TMA producer and warp 2 the weight producer.  Warp w runs on scheduler
+// w % 4 and may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so every group of
+// four consecutive warps covers the 128 lanes once.  Each scheduler carries one dequant
+// warp per group; the per-step control work (eight tcgen05.mma, costly to issue next
+// to busy dequant warps, the pair-row copy and the weight copies) is spread so that no
+// scheduler carries much more of it than the others.
 constexpr int kMmaWarp0 = 1;
-constexpr int kWeightTmaWarp = 4;
-constexpr int kEpiWarp0 = 5;
-constexpr int kDequantWarp0 = 9;
+constexpr int kEpiWarp0 = 4;
+constexpr int kDequantWarp0 = 8;
+__host__ __device__ constexpr int weight_tma_warp(bool bin) { return bin ? 0 : 2; }
+__host__ __device__ constexpr int pair_tma_warp(bool bin) { return bin ? -1 : 0; }
 __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWarp0 + 4 * groups) * 32; }
 
 // Two rings:
@@ -74,11 +76,11 @@ __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWar
 // (which may land out of order) can pass a wait early, and the rings desynchronise
 // (checked by simulating the protocol).
 //
-// Pair rows: with B3D the tile's rows of one K step (both 64-wide slabs) arrive in a
-// single 3-D box copy {64 elements, NMAX rows, 2 slabs}; otherwise as 2-D boxes of 16
-// rows x 64 elements, as many as the tile needs.  The copy instruction is issued from
-// one warp that also serves every step's barrier traffic, so fewer copies per step
-// shorten the loop that feeds the MMA.
+// Pair rows: with BIN the tile's rows of one K step (both 64-wide slabs) arrive in a
+// single 3-D box copy {64 elements, NMAX rows, 2 slabs}, issued by the MMA warp that
+// owns the step; otherwise a producer warp copies 2-D boxes of 16 rows x 64 elements,
+// as many as the tile needs.  One copy per step, from warps spread over the
+// schedulers, keeps copy issue off the path that feeds the MMA.
 template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW>
 struct Cfg {
   static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
@@ -104,10 +106,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool B3D, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool BIN, bool FC1>
 __global__ void __launch_bounds__(gemm_threads(DG), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW>;
+  // BIN: pair rows as one 3-D box {64, NMAX rows, 2 slabs} per step, copied by the MMA
+  // warps; otherwise 2-D boxes of 16 rows from a producer warp
+  constexpr int kWeightTmaWarp = weight_tma_warp(BIN);
+  constexpr int kPairTmaWarp = pair_tma_warp(BIN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kPairTmaWarp && lane == 0) prefetch_tmap(&tmap_b);
+  if (warp == (BIN ? kMmaWarp0 : kPairTmaWarp) && lane == 0) prefetch_tmap(&tmap_b);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -156,6 +162,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 
   const int nks = p.K / kBK;
   const int n_units = (*p.n_tiles) * p.nrb;
+  // this CTA's units u = blockIdx.x, blockIdx.x + gridDim.x, .. of nks steps each
+  const int my_units = blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const uint32_t total = (uint32_t)my_units * (uint32_t)nks;
 
   if (warp == kWeightTmaWarp) {
     // ------------------------------------------------------------ weight TMA producer
@@ -186,7 +195,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
       for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
     }
-  } else if (warp == kPairTmaWarp) {
+  } else if (!BIN && warp == kPairTmaWarp) {
     // ------------------------------------------------------------ pair-row TMA producer
     const uint32_t leader = elect_one();
     const uint64_t pol = l2_policy_evict_last();
@@ -195,7 +204,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int t = u / p.nrb;
       const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
-      const int nb16 = B3D ? NMAX / 16 : (rows + 15) >> 4;
+      const int nb16 = (rows + 15) >> 4;
       const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
       for (int ks = 0; ks < nks; ++ks, ++it) {
         const int s = it % SL;
@@ -206,15 +215,11 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         const uint32_t st = smem_u32(bring + s * C::kBBytes);
         const uint32_t fb = smem_u32(&sfull[s]);
         mbar_arrive_expect_tx_if(leader, fb, tx);
-        if constexpr (B3D) {
-          tma_load_3d_if(leader, st, &tmap_b, 0, start, 2 * ks, fb, pol);
-        } else {
 #pragma unroll
-          for (int sl = 0; sl < 2; ++sl)
-            for (int g = 0; g < nb16; ++g)
-              tma_load_2d_if(leader, st + sl * C::kBSlab + g * 2048, &tmap_b, ks * kBK + sl * 64,
-                             start + g * 16, fb, pol);
-        }
+        for (int sl = 0; sl < 2; ++sl)
+          for (int g = 0; g < nb16; ++g)
+            tma_load_2d_if(leader, st + sl * C::kBSlab + g * 2048, &tmap_b, ks * kBK + sl * 64,
+                           start + g * 16, fb, pol);
       }
     }
     if (!ok) {  // the pair rows of the last slots may still be landing
@@ -233,6 +238,34 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     const uint32_t bdesc_lo0 = (uint32_t)bdesc0, bdesc_hi = (uint32_t)(bdesc0 >> 32);
     uint32_t it = 0, local = 0;
     bool ok = true;
+    // BIN: the pair rows of global step g go into slot g % SL, whose previous step
+    // g - SL belongs to this warp too (SL % NMW == 0).  The copy for the warp's next
+    // step is issued right after the MMAs of the current one, when the slot's previous
+    // step (one own step back) has long completed: a step of lead for the copy.
+    uint32_t bg = (uint32_t)m, blu = 0, bks = (uint32_t)m;  // next copy: step, unit, K step
+    int bstart = 0;
+    const uint64_t bpol = l2_policy_evict_last();
+    auto issue_b = [&]() -> bool {
+      if (bg >= total) return true;
+      while (bks >= (uint32_t)nks) {
+        bks -= nks;
+        ++blu;
+      }
+      if (bks < (uint32_t)NMW || bg == (uint32_t)m) {  // entered a unit: its tile's first row
+        const int t = ((int)blockIdx.x + (int)blu * (int)gridDim.x) / p.nrb;
+        bstart = p.tiles[3 * t + 1];
+      }
+      const uint32_t sl = bg % SL;
+      if (!warp_wait(sempty_u + sl * 8, ((bg / SL) & 1) ^ 1, abort_flag, p.err)) return false;
+      const uint32_t fb = sfull_u + sl * 8;
+      mbar_arrive_expect_tx_if(leader, fb, (uint32_t)C::kBBytes);
+      tma_load_3d_if(leader, smem_u32(bring + sl * C::kBBytes), &tmap_b, 0, bstart, 2 * (int)bks,
+                     fb, bpol);
+      bg += NMW;
+      bks += NMW;
+      return true;
+    };
+    if constexpr (BIN) ok = issue_b();
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
       const int t = u / p.nrb;
       const int rows = p.tiles[3 * t + 2];
@@ -257,6 +290,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         mma_bf16_ts_step8(leader, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (C::kBBytes >> 4),
                           bdesc_hi, C::kBSlab >> 4, idesc, ks != ks0 ? 1u : 0u);
         tc_commit_if(leader, sempty_u + sl * 8);
+        if constexpr (BIN) {
+          if (!issue_b()) {
+            ok = false;
+            break;
+          }
+        }
       }
       it += nks;
       if (ok) tc_commit_if(leader, smem_u32(&accf[ab]));
@@ -264,17 +303,19 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // no MMA may still be running when TMEM is released
     tc_commit_if(leader, smem_u32(drain));
     drain_wait(smem_u32(drain), 0);
+    if (BIN && !ok) {  // the pair rows of the last slots may still be landing
+      const unsigned long long t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------------------ dequant warps (DG groups)
     const int grp = (warp - kDequantWarp0) >> 2;  // this group's steps: grp, grp + DG, ..
     const int q = warp & 3;                       // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;                // weight row of the 128-row block
-    // The dequant warps only walk the CTA's step sequence: units u = blockIdx.x,
-    // blockIdx.x + gridDim.x, .. of nks steps each.  RS and SL are multiples of DG, so
-    // the group meets the same ring residues on every lap (s, a) and the phase bits
-    // flip on each wrap.
-    const int my_units = blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const uint32_t total = (uint32_t)my_units * (uint32_t)nks;
+    // The dequant warps only walk the CTA's step sequence.  RS and SL are multiples of
+    // DG, so the group meets the same ring residues on every lap (s, a) and the phase
+    // bits flip on each wrap.
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
     for (uint32_t it = grp; it < total; it += DG) {
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;
@@ -392,10 +433,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   }
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool B3D, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool BIN, bool FC1>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW>;
-  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, B3D, FC1>;
+  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, BIN, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   k<<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(tmap, p);
