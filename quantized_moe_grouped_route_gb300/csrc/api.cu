@@ -47,9 +47,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Row-major bf16 [rows][cols] operand, boxes of 64 columns x 16 rows, 128-byte swizzle.
 // Tensor map over a row-major bf16 matrix [rows][cols] for the GEMM's pair rows.
 // box_rows == 0: 2-D, box 16 rows x 64 elements.  box_rows > 0: 3-D view
-// {64 elements, rows, cols / 64 slabs} (slab stride 128 bytes), box {64, box_rows, 2},
-// which lands in shared memory as [slab][row][64 elements].
-int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+// {64 elements, rows, cols / 64 slabs} (slab stride 128 bytes), box
+// {64, box_rows, box_slabs}, which lands in shared memory as [slab][row][64 elements].
+int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int box_rows,
+                   int box_slabs) {
   auto fn = encode_fn();
   if (!fn) return QMOE_ERR_CUDA;
   CUresult r;
@@ -64,7 +65,7 @@ int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int b
   } else {
     cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)cols / 64};
     cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_slabs};
     cuuint32_t estr[3] = {1, 1, 1};
     r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -245,9 +246,9 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   float* ypart = reinterpret_cast<float*>(ws + L.ypart);
 
   CUtensorMap map_x, map_h;
-  const int box_rows = gemm_b_box_rows(rsched);
-  if (make_tmap_rows(&map_x, xs, L.rows, H, box_rows) != QMOE_OK) return QMOE_ERR_CUDA;
-  if (make_tmap_rows(&map_h, h, L.rows, I, box_rows) != QMOE_OK) return QMOE_ERR_CUDA;
+  const int box_rows = gemm_b_box_rows(rsched), box_slabs = gemm_b_box_slabs(rsched);
+  if (make_tmap_rows(&map_x, xs, L.rows, H, box_rows, box_slabs) != QMOE_OK) return QMOE_ERR_CUDA;
+  if (make_tmap_rows(&map_h, h, L.rows, I, box_rows, box_slabs) != QMOE_OK) return QMOE_ERR_CUDA;
 
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;

@@ -34,7 +34,7 @@
 namespace qmoe {
 namespace {
 
-constexpr int kBK = 128;            // K per pipeline step
+constexpr int kBK = 128;            // K per weight block of the repacked layout
 constexpr int kCodeBytes = 8192;    // 128 rows x 128 K / 2
 constexpr int kScaleBytes = 1024;   // 128 rows x 8 blocks
 constexpr int kRawBytes = kCodeBytes + kScaleBytes;
@@ -81,15 +81,22 @@ __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWar
 // owns the step; otherwise a producer warp copies 2-D boxes of 16 rows x 64 elements,
 // as many as the tile needs.  One copy per step, from warps spread over the
 // schedulers, keeps copy issue off the path that feeds the MMA.
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW>
+// A pipeline step covers KS weight blocks (KS x 128 of K): KS x 9 KB of the weight ring,
+// a TMEM A slot of KS x 64 columns, 2 KS slabs of pair rows and 8 KS MMAs, so the
+// per-step barrier and bookkeeping work is paid once per KS blocks.  The last step of
+// a unit covers the remaining nb128 - (nss - 1) KS blocks ("halves").
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS>
 struct Cfg {
   static constexpr int kBSlab = NMAX * 128;  // one 64-wide K slab of B: NMAX rows x 128 bytes
-  static constexpr int kBBytes = 2 * kBSlab;
-  static constexpr int kAccCol0 = SL * 64;   // TMEM: [A slots: 64 cols][acc: ACCB x NMW x NMAX]
-  static constexpr int kSmemBytes = SL * kBBytes + RS * kRawBytes + 1024 + kCtrlBytes;
+  static constexpr int kBBytes = 2 * KS * kBSlab;
+  static constexpr int kStageBytes = KS * kRawBytes;  // [KS codes blocks][KS scale blocks]
+  static constexpr int kSlotCols = 64 * KS;
+  static constexpr int kAccCol0 = SL * kSlotCols;  // TMEM: [A slots][acc: ACCB x NMW x NMAX]
+  static constexpr int kSmemBytes = SL * kBBytes + RS * kStageBytes + 1024 + kCtrlBytes;
   static constexpr int kThreads = gemm_threads(DG);
-  static_assert(kBBytes % 1024 == 0 && kRawBytes % 1024 == 0, "1024-byte stage alignment");
-  static_assert(SL * 64 + ACCB * NMW * NMAX <= kTmemCols, "TMEM budget");
+  static_assert(KS == 1 || KS == 2, "weight blocks per step");
+  static_assert(kBBytes % 1024 == 0 && kStageBytes % 1024 == 0, "1024-byte stage alignment");
+  static_assert(SL * kSlotCols + ACCB * NMW * NMAX <= kTmemCols, "TMEM budget");
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
   static_assert(NMW >= 1 && NMW <= 3, "MMA warps 1..3");
   static_assert(SL % DG == 0 && SL % NMW == 0, "each slot needs one dequant group and one MMA warp");
@@ -106,20 +113,21 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool BIN, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1>
 __global__ void __launch_bounds__(gemm_threads(DG), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW>;
-  // BIN: pair rows as one 3-D box {64, NMAX rows, 2 slabs} per step, copied by the MMA
-  // warps; otherwise 2-D boxes of 16 rows from a producer warp
+  using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW, KS>;
+  static_assert(BIN || KS == 1, "2-D pair-row boxes are issued per 128-wide block");
+  // BIN: pair rows as one 3-D box {64, NMAX rows, 2 KS slabs} per step, copied by the
+  // MMA warps; otherwise 2-D boxes of 16 rows from a producer warp
   constexpr int kWeightTmaWarp = weight_tma_warp(BIN);
   constexpr int kPairTmaWarp = pair_tma_warp(BIN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bring = smem;                          // [SL][kBBytes] pair rows
-  uint8_t* rring = smem + SL * C::kBBytes;        // [RS][kRawBytes]
-  uint8_t* ctrl = rring + RS * kRawBytes;
+  uint8_t* rring = smem + SL * C::kBBytes;        // [RS][kStageBytes]
+  uint8_t* ctrl = rring + RS * C::kStageBytes;
   uint64_t* rfull = reinterpret_cast<uint64_t*>(ctrl);  // raw step landed (tx)
   uint64_t* rempty = rfull + RS;                        // raw step read by 4 dequant warps
   uint64_t* sfull = rempty + RS;                        // slot: 4 dequant warps + pair rows (tx)
@@ -160,7 +168,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int nks = p.K / kBK;
+  const int nb128 = p.K / kBK;            // 128-wide weight blocks per unit
+  const int nks = (nb128 + KS - 1) / KS;  // pipeline steps per unit
+  const int last_halves = nb128 - (nks - 1) * KS;
   const int n_units = (*p.n_tiles) * p.nrb;
   // this CTA's units u = blockIdx.x, blockIdx.x + gridDim.x, .. of nks steps each
   const int my_units = blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -176,19 +186,21 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t];
-      const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nks;
+      const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nb128;
       for (int ks = 0; ks < nks; ++ks, ++it) {
         const int s = it % RS;
         if (!warp_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint32_t st = smem_u32(rring + s * kRawBytes);
+        const uint32_t nh = ks == nks - 1 ? (uint32_t)last_halves : (uint32_t)KS;
+        const size_t b0 = blk + (size_t)ks * KS;
+        const uint32_t st = smem_u32(rring + s * C::kStageBytes);
         const uint32_t fb = smem_u32(&rfull[s]);
-        mbar_arrive_expect_tx_if(leader, fb, kRawBytes);
-        bulk_g2s_if(leader, st, p.wcodes + (blk + ks) * kCodeBytes, kCodeBytes, fb, pol);
-        bulk_g2s_if(leader, st + kCodeBytes, p.wscales + (blk + ks) * kScaleBytes, kScaleBytes, fb,
-                    pol);
+        mbar_arrive_expect_tx_if(leader, fb, nh * kRawBytes);
+        bulk_g2s_if(leader, st, p.wcodes + b0 * kCodeBytes, nh * kCodeBytes, fb, pol);
+        bulk_g2s_if(leader, st + KS * kCodeBytes, p.wscales + b0 * kScaleBytes, nh * kScaleBytes,
+                    fb, pol);
       }
     }
     if (!ok) {  // let the copies already issued land before the CTA can exit
@@ -259,8 +271,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       if (!warp_wait(sempty_u + sl * 8, ((bg / SL) & 1) ^ 1, abort_flag, p.err)) return false;
       const uint32_t fb = sfull_u + sl * 8;
       mbar_arrive_expect_tx_if(leader, fb, (uint32_t)C::kBBytes);
-      tma_load_3d_if(leader, smem_u32(bring + sl * C::kBBytes), &tmap_b, 0, bstart, 2 * (int)bks,
-                     fb, bpol);
+      tma_load_3d_if(leader, smem_u32(bring + sl * C::kBBytes), &tmap_b, 0, bstart,
+                     2 * KS * (int)bks, fb, bpol);
       bg += NMW;
       bks += NMW;
       return true;
@@ -287,8 +299,13 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           break;
         }
         tc_fence_after();
-        mma_bf16_ts_step8(leader, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (C::kBBytes >> 4),
-                          bdesc_hi, C::kBSlab >> 4, idesc, ks != ks0 ? 1u : 0u);
+        mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols,
+                          bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4, idesc,
+                          ks != ks0 ? 1u : 0u);
+        if (KS == 2 && (ks != nks - 1 || last_halves == 2))
+          mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols + 64,
+                            bdesc_lo0 + ((sl * C::kBBytes + 2 * C::kBSlab) >> 4), bdesc_hi,
+                            C::kBSlab >> 4, idesc, 1u);
         tc_commit_if(leader, sempty_u + sl * 8);
         if constexpr (BIN) {
           if (!issue_b()) {
@@ -317,32 +334,47 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // DG, so the group meets the same ring residues on every lap (s, a) and the phase
     // bits flip on each wrap.
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
+    uint32_t pos = (uint32_t)grp % (uint32_t)nks;  // step of the current one within its unit
     for (uint32_t it = grp; it < total; it += DG) {
+      const int nh = (KS == 2 && pos == (uint32_t)nks - 1) ? last_halves : KS;
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;
-      const uint8_t* st = rring + s * kRawBytes;
-      const uint4* codes = reinterpret_cast<const uint4*>(st);
-      uint4 cw[4];
+      const uint8_t* st = rring + s * C::kStageBytes;
+      uint4 cw[KS][4];
+      uint2 sc[KS];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) cw[kk] = codes[kk * 128 + row];
-      const uint2 sc = *reinterpret_cast<const uint2*>(st + kCodeBytes + row * 8);
-      // the row's 8 block scales as bf16x2 multipliers, all looked up before the first
-      // TMEM store (whose ordering constraint would otherwise serialize the lookups)
-      uint32_t sv[8];
+      for (int h = 0; h < KS; ++h) {
+        if (h < nh) {
+          const uint4* codes = reinterpret_cast<const uint4*>(st + h * kCodeBytes);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sv[j] = scale_lut[((j < 4 ? sc.x : sc.y) >> (8 * (j & 3))) & 0xFF];
+          for (int kk = 0; kk < 4; ++kk) cw[h][kk] = codes[kk * 128 + row];
+          sc[h] = *reinterpret_cast<const uint2*>(st + KS * kCodeBytes + h * kScaleBytes + row * 8);
+        }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw step may be refilled
+      if (lane == 0) mbar_arrive(smem_u32(&rempty[s]));  // the raw stage may be refilled
       if (!warp_wait(smem_u32(&sempty[a]), aph ^ 1, abort_flag, p.err)) break;
       tc_fence_after();
-      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * 64;
+      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * C::kSlotCols;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t o[16];
-        dequant8(cw[kk].x, sv[2 * kk], o + 0);
-        dequant8(cw[kk].y, sv[2 * kk], o + 4);
-        dequant8(cw[kk].z, sv[2 * kk + 1], o + 8);
-        dequant8(cw[kk].w, sv[2 * kk + 1], o + 12);
-        tmem_st_x16(ta + kk * 16, o);
+      for (int h = 0; h < KS; ++h) {
+        if (h < nh) {
+          // the row's 8 block scales as bf16x2 multipliers, looked up before the first
+          // TMEM store of the block (whose ordering constraint would otherwise
+          // serialize the lookups)
+          uint32_t sv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            sv[j] = scale_lut[((j < 4 ? sc[h].x : sc[h].y) >> (8 * (j & 3))) & 0xFF];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint32_t o[16];
+            dequant8(cw[h][kk].x, sv[2 * kk], o + 0);
+            dequant8(cw[h][kk].y, sv[2 * kk], o + 4);
+            dequant8(cw[h][kk].z, sv[2 * kk + 1], o + 8);
+            dequant8(cw[h][kk].w, sv[2 * kk + 1], o + 12);
+            tmem_st_x16(ta + h * 64 + kk * 16, o);
+          }
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -352,6 +384,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       if (s >= (uint32_t)RS) { s -= RS; rph ^= 1; }
       a += DG;
       if (a >= (uint32_t)SL) { a -= SL; aph ^= 1; }
+      pos += DG;
+      while (pos >= (uint32_t)nks) pos -= nks;
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ------------------------------------------------------------ epilogue warps
@@ -433,10 +467,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   }
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, bool BIN, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
-  using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW>;
-  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, BIN, FC1>;
+  using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW, KS>;
+  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, KS, BIN, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   k<<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(tmap, p);
@@ -449,18 +483,21 @@ int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 256; }
 
 int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 0; }
 
-// decode : tiles <= 16 pairs, 15 weight steps in flight (135 KB), 6 slots, 3 MMA warps
-//          x 2 accumulator buffers, 3 dequant groups, pair rows as one 3-D box per step
+int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
+
+// decode : tiles <= 16 pairs, steps of 2 weight blocks (256 of K), 9 steps in flight
+//          (162 KB), 3 slots, 3 MMA warps x 2 accumulator buffers, 3 dequant groups, pair
+//          rows as one 3-D box per step
 // prefill: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair rows each),
 //          1 MMA warp, 1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 16 rows
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
   if (sched == QMOE_SCHED_DECODE)
-    return fc1 ? run<16, 15, 6, 2, 3, 3, true, true>(tmap_b, p, num_sms, stream)
-               : run<16, 15, 6, 2, 3, 3, true, false>(tmap_b, p, num_sms, stream);
-  return fc1 ? run<256, 8, 2, 1, 2, 1, false, true>(tmap_b, p, num_sms, stream)
-             : run<256, 8, 2, 1, 2, 1, false, false>(tmap_b, p, num_sms, stream);
+    return fc1 ? run<16, 9, 3, 2, 3, 3, 2, true, true>(tmap_b, p, num_sms, stream)
+               : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<256, 8, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
+             : run<256, 8, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
 }
 
 }  // namespace qmoe
