@@ -102,7 +102,7 @@ struct Cfg {
   static_assert(SL % DG == 0 && SL % NMW == 0, "each slot needs one dequant group and one MMA warp");
   static_assert(RS % DG == 0, "each weight stage needs one dequant group");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert((2 * (RS + SL + ACCB) + 1) * 8 + 16 <= 1024, "barrier area");
+  static_assert((2 * RS + SL * (KS + 1) + 2 * ACCB + 1) * 8 + 16 <= 1024, "barrier area");
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -130,8 +130,11 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   uint8_t* ctrl = rring + RS * C::kStageBytes;
   uint64_t* rfull = reinterpret_cast<uint64_t*>(ctrl);  // raw step landed (tx)
   uint64_t* rempty = rfull + RS;                        // raw step read by 4 dequant warps
-  uint64_t* sfull = rempty + RS;                        // slot: 4 dequant warps + pair rows (tx)
-  uint64_t* sempty = sfull + SL;                        // slot read by the MMAs
+  // sfull[slot * KS + h]: block h of the slot stored by the 4 dequant warps (block 0
+  // also waits for the pair rows' bytes), so the MMAs of block 0 can start while the
+  // dequant warps still work on block 1
+  uint64_t* sfull = rempty + RS;
+  uint64_t* sempty = sfull + SL * KS;                   // slot read by the MMAs
   uint64_t* accf = sempty + SL;                         // accumulators ready (NMW commits)
   uint64_t* acce = accf + ACCB;                         // accumulators drained (4 warps)
   uint64_t* drain = acce + ACCB;
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       mbar_init(smem_u32(&rempty[s]), 4);
     }
     for (int s = 0; s < SL; ++s) {
-      mbar_init(smem_u32(&sfull[s]), 5);
+      for (int h = 0; h < KS; ++h) mbar_init(smem_u32(&sfull[s * KS + h]), h == 0 ? 5 : 4);
       mbar_init(smem_u32(&sempty[s]), 1);
     }
     for (int a = 0; a < ACCB; ++a) {
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           break;
         }
         const uint32_t st = smem_u32(bring + s * C::kBBytes);
-        const uint32_t fb = smem_u32(&sfull[s]);
+        const uint32_t fb = smem_u32(&sfull[s * KS]);
         mbar_arrive_expect_tx_if(leader, fb, tx);
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       }
       const uint32_t sl = bg % SL;
       if (!warp_wait(sempty_u + sl * 8, ((bg / SL) & 1) ^ 1, abort_flag, p.err)) return false;
-      const uint32_t fb = sfull_u + sl * 8;
+      const uint32_t fb = sfull_u + sl * KS * 8;
       mbar_arrive_expect_tx_if(leader, fb, (uint32_t)C::kBBytes);
       tma_load_3d_if(leader, smem_u32(bring + sl * C::kBBytes), &tmap_b, 0, bstart,
                      2 * KS * (int)bks, fb, bpol);
@@ -294,7 +297,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       for (int ks = ks0; ks < nks; ks += NMW) {
         const uint32_t sit = it + (uint32_t)ks;
         const int sl = sit % SL;
-        if (!warp_wait(sfull_u + sl * 8, (sit / SL) & 1, abort_flag, p.err)) {
+        const uint32_t sph = (sit / SL) & 1;
+        if (!warp_wait(sfull_u + sl * KS * 8, sph, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -302,10 +306,16 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols,
                           bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4, idesc,
                           ks != ks0 ? 1u : 0u);
-        if (KS == 2 && (ks != nks - 1 || last_halves == 2))
+        if (KS == 2 && (ks != nks - 1 || last_halves == 2)) {
+          if (!warp_wait(sfull_u + (sl * KS + 1) * 8, sph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols + 64,
                             bdesc_lo0 + ((sl * C::kBBytes + 2 * C::kBSlab) >> 4), bdesc_hi,
                             C::kBSlab >> 4, idesc, 1u);
+        }
         tc_commit_if(leader, sempty_u + sl * 8);
         if constexpr (BIN) {
           if (!issue_b()) {
@@ -374,12 +384,14 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
             dequant8(cw[h][kk].w, sv[2 * kk + 1], o + 12);
             tmem_st_x16(ta + h * 64 + kk * 16, o);
           }
+          tmem_wait_st();
+          tc_fence_before();
         }
+        // a block past the unit's end is left unwritten, but its barrier still
+        // completes so that every slot barrier advances once per use
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sfull[a * KS + h]));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sfull[a]));
       s += DG;
       if (s >= (uint32_t)RS) { s -= RS; rph ^= 1; }
       a += DG;
