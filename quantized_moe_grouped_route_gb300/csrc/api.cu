@@ -46,7 +46,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Row-major bf16 [rows][cols] operand, boxes of 64 columns x 16 rows, 128-byte swizzle.
 // Tensor map over a row-major bf16 matrix [rows][cols] for the GEMM's pair rows.
-// box_rows == 0: 2-D, box 16 rows x 64 elements.  box_rows > 0: 3-D view
+// box_slabs == 0: 2-D, box box_rows rows x 64 elements.  box_slabs > 0: 3-D view
 // {64 elements, rows, cols / 64 slabs} (slab stride 128 bytes), box
 // {64, box_rows, box_slabs}, which lands in shared memory as [slab][row][64 elements].
 int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int box_rows,
@@ -54,10 +54,10 @@ int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int b
   auto fn = encode_fn();
   if (!fn) return QMOE_ERR_CUDA;
   CUresult r;
-  if (box_rows == 0) {
+  if (box_slabs == 0) {
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, 16};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -52,6 +52,7 @@ constexpr int kCtrlBytes = 2048;    // barriers, TMEM slot, abort flag, scale ta
 // scheduler carries much more of it than the others.
 constexpr int kMmaWarp0 = 1;
 constexpr int kEpiWarp0 = 4;
+constexpr int kPairBoxRows = 64;  // rows of a 2-D pair-row box (prefill schedule)
 constexpr int kDequantWarp0 = 8;
 __host__ __device__ constexpr int weight_tma_warp(bool bin) { return bin ? 0 : 2; }
 __host__ __device__ constexpr int pair_tma_warp(bool bin) { return bin ? -1 : 0; }
@@ -78,8 +79,8 @@ __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWar
 //
 // Pair rows: with BIN the tile's rows of one K step (both 64-wide slabs) arrive in a
 // single 3-D box copy {64 elements, NMAX rows, 2 slabs}, issued by the MMA warp that
-// owns the step; otherwise a producer warp copies 2-D boxes of 16 rows x 64 elements,
-// as many as the tile needs.  One copy per step, from warps spread over the
+// owns the step; otherwise a producer warp copies 2-D boxes of kPairBoxRows rows x 64
+// elements, as many as the tile needs.  One copy per step, from warps spread over the
 // schedulers, keeps copy issue off the path that feeds the MMA.
 // A pipeline step covers KS weight blocks (KS x 128 of K): KS x 9 KB of the weight ring,
 // a TMEM A slot of KS x 64 columns, 2 KS slabs of pair rows and 8 KS MMAs, so the
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int t = u / p.nrb;
       const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
-      const int nb16 = (rows + 15) >> 4;
-      const uint32_t tx = 2u * (uint32_t)nb16 * 2048u;
+      const int nbox = (rows + kPairBoxRows - 1) / kPairBoxRows;
+      const uint32_t tx = 2u * (uint32_t)nbox * (uint32_t)(kPairBoxRows * 128);
       for (int ks = 0; ks < nks; ++ks, ++it) {
         const int s = it % SL;
         if (!warp_wait(smem_u32(&sempty[s]), ((it / SL) & 1) ^ 1, abort_flag, p.err)) {
@@ -232,9 +233,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         mbar_arrive_expect_tx_if(leader, fb, tx);
 #pragma unroll
         for (int sl = 0; sl < 2; ++sl)
-          for (int g = 0; g < nb16; ++g)
-            tma_load_2d_if(leader, st + sl * C::kBSlab + g * 2048, &tmap_b, ks * kBK + sl * 64,
-                           start + g * 16, fb, pol);
+          for (int g = 0; g < nbox; ++g)
+            tma_load_2d_if(leader, st + sl * C::kBSlab + g * kPairBoxRows * 128, &tmap_b,
+                           ks * kBK + sl * 64, start + g * kPairBoxRows, fb, pol);
       }
     }
     if (!ok) {  // the pair rows of the last slots may still be landing
@@ -493,7 +494,7 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 
 int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 256; }
 
-int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 0; }
+int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : kPairBoxRows; }
 
 int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
 

@@ -48,8 +48,8 @@ enum class GemmKind { kFc1, kFc2 };
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream);
 int gemm_tile_n(int sched);  // max pairs per tile for a schedule
-// Rows and 64-wide slabs of the 3-D pair-row box {64 elements, rows, slabs} the GEMM of
-// a schedule loads per pipeline step, or 0 when it loads 2-D boxes of 16 rows x 64
+// Rows and 64-wide slabs of the pair-row box the GEMM of a schedule loads: a 3-D box
+// {64 elements, rows, slabs} per pipeline step, or (slabs 0) 2-D boxes of rows x 64
 // elements.
 int gemm_b_box_rows(int sched);
 int gemm_b_box_slabs(int sched);
