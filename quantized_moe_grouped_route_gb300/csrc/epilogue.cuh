@@ -1,0 +1,60 @@
+// GEMM epilogue for one chunk of 16 accumulator columns (pairs c0 .. c0+15 of a tile)
+// of one TMEM lane quarter: the lane holds weight row q*32 + lane of row block rb.
+//   FC1: lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
+//        intermediate indices; h = bf16(SiLU(gate) * up) of each valid pair.
+//   FC2: ypart[pair][row] = acc * global scale * routing weight.
+// gsc is the expert's global scale times 2^7 (undoing the dequant's 2^-7).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace qmoe {
+
+template <bool FC1>
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const float (&v)[16], int lane,
+                                               int q, int rb, int start, int rows, int c0,
+                                               float gsc) {
+  if constexpr (FC1) {
+    // lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
+    // intermediate indices.  For each pair of columns (c, c+1) the lanes trade
+    // one value so that lane j < 16 forms h(i, c) and lane j + 16 forms
+    // h(i, c+1): every lane computes and stores.
+    const bool is_up = lane < 16;
+    const int i = rb * 64 + q * 16 + (lane & 15);
+    __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const float send = (is_up ? v[c + 1] : v[c]) * gsc;
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      const float up = is_up ? v[c] * gsc : recv;
+      const float gate = is_up ? recv : v[c + 1] * gsc;
+      const int col = c0 + c + (is_up ? 0 : 1);
+      if (col < rows) {
+        const float hv = gate / (1.0f + expf(-gate)) * up;
+        hp[(size_t)(start + col) * p.I + i] = __float2bfloat16_rn(hv);
+      }
+    }
+  } else {
+    // the chunk's 16 pair ids and routing weights: one coalesced load, then
+    // broadcast by shuffles
+    const int cl = lane & 15;
+    int my_pair = 0;
+    float my_w = 0.f;
+    if (c0 + cl < rows) {
+      my_pair = p.sorted_pair[start + c0 + cl];
+      my_w = p.topk_w[my_pair] * gsc;
+    }
+    const int jrow = rb * 128 + q * 32 + lane;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int pair = __shfl_sync(0xffffffffu, my_pair, c);
+      const float w = __shfl_sync(0xffffffffu, my_w, c);
+      if (c0 + c < rows) p.ypart[(size_t)pair * p.H + jrow] = v[c] * w;
+    }
+  }
+}
+
+}  // namespace qmoe

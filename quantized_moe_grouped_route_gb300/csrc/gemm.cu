@@ -29,6 +29,7 @@
 // drained with bounded waits, and TMEM is released before the CTA exits.
 #include "common.cuh"
 #include "dequant.cuh"
+#include "epilogue.cuh"
 #include "launch.h"
 
 namespace qmoe {
@@ -427,44 +428,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
         }
-        if constexpr (FC1) {
-          // lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
-          // intermediate indices.  For each pair of columns (c, c+1) the lanes trade
-          // one value so that lane j < 16 forms h(i, c) and lane j + 16 forms
-          // h(i, c+1): every lane computes and stores.
-          const bool is_up = lane < 16;
-          const int i = rb * 64 + q * 16 + (lane & 15);
-          __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
-#pragma unroll
-          for (int c = 0; c < 16; c += 2) {
-            const float send = (is_up ? v[c + 1] : v[c]) * gsc;
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float up = is_up ? v[c] * gsc : recv;
-            const float gate = is_up ? recv : v[c + 1] * gsc;
-            const int col = c0 + c + (is_up ? 0 : 1);
-            if (col < rows) {
-              const float hv = gate / (1.0f + expf(-gate)) * up;
-              hp[(size_t)(start + col) * p.I + i] = __float2bfloat16_rn(hv);
-            }
-          }
-        } else {
-          // the chunk's 16 pair ids and routing weights: one coalesced load, then
-          // broadcast by shuffles
-          const int cl = lane & 15;
-          int my_pair = 0;
-          float my_w = 0.f;
-          if (c0 + cl < rows) {
-            my_pair = p.sorted_pair[start + c0 + cl];
-            my_w = p.topk_w[my_pair] * gsc;
-          }
-          const int jrow = rb * 128 + q * 32 + lane;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int pair = __shfl_sync(0xffffffffu, my_pair, c);
-            const float w = __shfl_sync(0xffffffffu, my_w, c);
-            if (c0 + c < rows) p.ypart[(size_t)pair * p.H + jrow] = v[c] * w;
-          }
-        }
+        epilogue_chunk<FC1>(p, v, lane, q, rb, start, rows, c0, gsc);
       }
       tc_fence_before();
       __syncwarp();
