@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--sched", choices=["auto", "decode", "prefill"], default="auto")
+    ap.add_argument("--sched", choices=["auto", "decode", "prefill", "prefill_pair"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the untimed clock-sampling soak (for profiler launch lists)")
@@ -227,7 +227,8 @@ def ours_arm(args, rank, world, local):
         dist.init_process_group("nccl", device_id=dev)
     cfg = config_by_name(args.config)
     sched = {"auto": qmoe.QMOE_SCHED_AUTO, "decode": qmoe.QMOE_SCHED_DECODE,
-             "prefill": qmoe.QMOE_SCHED_PREFILL}[args.sched]
+             "prefill": qmoe.QMOE_SCHED_PREFILL,
+             "prefill_pair": qmoe.QMOE_SCHED_PREFILL_PAIR}[args.sched]
     li = make_inputs(cfg, dev, token_seed=cfg.seed + 1000 * rank)
     torch.cuda.synchronize()
 

@@ -51,6 +51,10 @@ extern "C" {
 #define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
 #define QMOE_SCHED_DECODE 1  /* tiles of <= 16 pairs: weight streaming, HBM bound */
 #define QMOE_SCHED_PREFILL 2 /* tiles of <= 256 pairs: tensor bound */
+/* As PREFILL, with each 256-row weight tile on a pair of SMs (tcgen05 2-CTA MMAs, each
+   SM holding half of the tile's pair rows); a GEMM whose count of 128-row weight blocks
+   is odd runs as PREFILL.  Same results as PREFILL; slower than it at present. */
+#define QMOE_SCHED_PREFILL_PAIR 3
 
 /* Weight roles for moe_nvfp4_repack. */
 #define QMOE_W13 1 /* w13 [E][2I][H/2]: up and gate rows, interleaved for the SwiGLU epilogue */

@@ -8,4 +8,5 @@ from .qmoe import (  # noqa: F401
     NVFP4MoE, QmoeError, moe_nvfp4_forward, moe_nvfp4_repack, moe_route, qmoe_forward_workspace_size,
     qmoe_max_tiles, qmoe_read_error, qmoe_repacked_fp4_size, qmoe_repacked_scale_size,
     qmoe_route_workspace_size, qmoe_sched_tile_n, qmoe_selftest_dequant, qmoe_selftest_timeout,
-    QMOE_SCHED_AUTO, QMOE_SCHED_DECODE, QMOE_SCHED_PREFILL, QMOE_W13, QMOE_W2)
+    QMOE_SCHED_AUTO, QMOE_SCHED_DECODE, QMOE_SCHED_PREFILL, QMOE_SCHED_PREFILL_PAIR, QMOE_W13,
+    QMOE_W2)

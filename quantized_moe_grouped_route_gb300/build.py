@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libqmoe.so")
 
-SOURCES = ["api.cu", "route.cu", "misc.cu", "gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "misc.cu", "gemm.cu", "gemm2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

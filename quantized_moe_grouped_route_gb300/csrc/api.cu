@@ -90,7 +90,8 @@ int check_shape(int M, int H, int I, int E, int top_k) {
 }
 
 int resolve_sched(int sched, int M, int top_k, int E) {
-  if (sched == QMOE_SCHED_DECODE || sched == QMOE_SCHED_PREFILL) return sched;
+  if (sched == QMOE_SCHED_DECODE || sched == QMOE_SCHED_PREFILL || sched == QMOE_SCHED_PREFILL_PAIR)
+    return sched;
   return (long long)M * top_k <= 4LL * E ? QMOE_SCHED_DECODE : QMOE_SCHED_PREFILL;
 }
 
@@ -216,7 +217,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
                         size_t ws_bytes, void* stream, void* const* events) {
   int rc = check_shape(M, H, I, E, top_k);
   if (rc != QMOE_OK) return rc;
-  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL) return QMOE_ERR_ARG;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
   if (M == 0) return QMOE_OK;
   if (!x_dev || !w13_fp4_dev || !w13_scale_dev || !w13_gscale_dev || !w2_fp4_dev ||
       !w2_scale_dev || !w2_gscale_dev || !topk_ids_dev || !topk_weights_dev || !out_dev ||
@@ -301,7 +302,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
 int qmoe_forward_workspace_layout(int M, int H, int I, int E, int top_k, int sched,
                                   size_t* layout_out) {
   if (!layout_out) return QMOE_ERR_ARG;
-  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL) return QMOE_ERR_ARG;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
   int rc = check_shape(M, H, I, E, top_k);
   if (rc != QMOE_OK) return rc;
   const ForwardLayout L = forward_layout(M, H, I, E, top_k, sched);
@@ -330,7 +331,7 @@ int moe_nvfp4_forward_noalloc(const void* x_dev, const uint8_t* w13_fp4_dev,
                               int E, int top_k, int sched, void* stream) {
   int rc = check_shape(M, H, I, E, top_k);
   if (rc != QMOE_OK) return rc;
-  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL) return QMOE_ERR_ARG;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
   if (M == 0) return QMOE_OK;
   if (forward_layout(M, H, I, E, top_k, sched).total > (size_t)QMOE_NOALLOC_SCRATCH_BYTES)
     return QMOE_ERR_WORKSPACE;  // this batch needs more scratch than the built-in array

@@ -164,6 +164,16 @@ __device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, cons
       : "memory");
 }
 
+// Prefetch of a 2-D tensor box into L2 by one lane (pred != 0), no shared memory
+// involved; x (innermost) must be a multiple of 8 bf16 elements.
+__device__ __forceinline__ void tma_prefetch_2d_if(uint32_t pred, const CUtensorMap* map, int x, int y) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%1, {%2, %3}];\n\t}" ::"r"(pred),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+      : "memory");
+}
+
 // 3-D tiled tensor copy by one lane (pred != 0); x (innermost) must be a multiple of
 // 8 bf16 elements.
 __device__ __forceinline__ void tma_load_3d_if(uint32_t pred, uint32_t dst, const CUtensorMap* map,
@@ -304,6 +314,18 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// tcgen05.ld writes its registers asynchronously: they hold the data only after
+// tcgen05.wait::ld.  The compiler sees the load's outputs as ready at once, so after
+// the wait each loaded array goes through this empty statement, which it must treat as
+// rewriting the registers: no use of them can then be scheduled above the wait.
+__device__ __forceinline__ void tmem_ld_ready(uint32_t (&v)[16]) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
+               :
+               : "memory");
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.

@@ -1,9 +1,14 @@
-// GEMM epilogue for one chunk of 16 accumulator columns (pairs c0 .. c0+15 of a tile)
-// of one TMEM lane quarter: the lane holds weight row q*32 + lane of row block rb.
+// GEMM epilogue for chunks of 16 accumulator columns (pairs c0 .. c0+15 of a tile) of
+// one TMEM lane quarter: the lane holds weight row q*32 + lane of row block rb.
 //   FC1: lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
 //        intermediate indices; h = bf16(SiLU(gate) * up) of each valid pair.
 //   FC2: ypart[pair][row] = acc * global scale * routing weight.
 // gsc is the expert's global scale times 2^7 (undoing the dequant's 2^-7).
+//
+// epilogue_chunk_fc1 computes its 8 column results independently of each other and
+// free of branches: on the prefill schedule the epilogue of a unit stalls the MMA (one
+// accumulator per unit), so it must run at instruction throughput, not at the latency
+// of one column at a time.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -13,10 +18,46 @@
 
 namespace qmoe {
 
+// SiLU(g) * up with e^-g taken as 2^(-g log2 e) and one approximate division; the
+// result is rounded to bf16 afterwards.  For g below about -88, e^-g overflows and the
+// value returned is 0 (the exact value is below 1e-36).
+__device__ __forceinline__ float silu_mul(float gate, float up) {
+  const float e = exp2f(gate * -1.4426950408889634f);
+  return __fdividef(gate, 1.0f + e) * up;
+}
+
+__device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const float (&v)[16],
+                                                   int lane, int q, int rb, int start, int rows,
+                                                   int c0, float gsc) {
+  // For each pair of columns (c, c+1) the lanes trade one value so that lane j < 16
+  // forms h(i, c) and lane j + 16 forms h(i, c+1): every lane computes and stores.
+  const bool is_up = lane < 16;
+  const int i = rb * 64 + q * 16 + (lane & 15);
+  __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
+  float hv[8];
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const float send = (is_up ? v[c + 1] : v[c]) * gsc;
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    const float up = is_up ? v[c] * gsc : recv;
+    const float gate = is_up ? recv : v[c + 1] * gsc;
+    hv[c >> 1] = silu_mul(gate, up);
+  }
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const int col = c0 + c + (is_up ? 0 : 1);
+    if (col < rows) hp[(size_t)(start + col) * p.I + i] = __float2bfloat16_rn(hv[c >> 1]);
+  }
+}
+
+// Chunk epilogue that reads the chunk's pair ids and routing weights itself (FC2) and
+// forms the SiLU with expf and an IEEE division (FC1).  The decode schedule uses it for
+// both GEMMs (there the epilogue overlaps the next unit's MMAs, and this form kept the
+// dequant loop fastest), the prefill schedules for FC2.
 template <bool FC1>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const float (&v)[16], int lane,
-                                               int q, int rb, int start, int rows, int c0,
-                                               float gsc) {
+__device__ __forceinline__ void epilogue_chunk_small(const GemmParams& p, const float (&v)[16],
+                                                     int lane, int q, int rb, int start, int rows,
+                                                     int c0, float gsc) {
   if constexpr (FC1) {
     // lanes 0..15 hold up rows, lanes 16..31 the gate rows of the same 16
     // intermediate indices.  For each pair of columns (c, c+1) the lanes trade

@@ -404,31 +404,80 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;
+    constexpr int NCH = NMAX / 16;          // 16-column chunks of a tile
+    constexpr int G = NMW == 1 ? 4 : 1;     // chunks per TMEM round trip
     uint32_t local = 0, it0 = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local, it0 += nks) {
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
+      const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
       if (!warp_wait(smem_u32(&accf[ab]), (local / ACCB) & 1, abort_flag, p.err)) break;
       tc_fence_after();
-      const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
       const uint32_t tbase =
           tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMW * NMAX;
-      for (int c0 = 0; c0 < rows; c0 += 16) {
-        float v[16];
+      if constexpr (BIN) {
+        for (int c0 = 0; c0 < rows; c0 += 16) {
+          float v[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = 0.f;
-        // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this unit
-        // iff its first step ks0 = (m - it0 % NMW) mod NMW lies inside the unit
-        for (int m = 0; m < NMW; ++m) {
-          if ((m - (int)(it0 % NMW) + NMW) % NMW >= nks) continue;
-          uint32_t r[16];
-          tmem_ld_x16(tbase + m * NMAX + c0, r);
+          for (int c = 0; c < 16; ++c) v[c] = 0.f;
+          // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this unit
+          // iff its first step ks0 = (m - it0 % NMW) mod NMW lies inside the unit
+          for (int m = 0; m < NMW; ++m) {
+            if ((m - (int)(it0 % NMW) + NMW) % NMW >= nks) continue;
+            uint32_t r[16];
+            tmem_ld_x16(tbase + m * NMAX + c0, r);
+            tmem_wait_ld();
+            tmem_ld_ready(r);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
+          }
+          epilogue_chunk_small<FC1>(p, v, lane, q, rb, start, rows, c0, gsc);
+        }
+      } else {
+        // warp m holds MMAs of this unit iff its first step ks0 = (m - it0 % NMW) mod NMW
+        // lies inside the unit; accumulators are added in the fixed order m = 0, 1, ..
+        bool has[NMW];
+#pragma unroll
+        for (int m = 0; m < NMW; ++m) has[m] = (m - (int)(it0 % NMW) + NMW) % NMW < nks;
+#pragma unroll
+        for (int k0 = 0; k0 < NCH; k0 += G) {
+          if (16 * k0 >= rows) break;
+          uint32_t r[NMW][G][16];
+#pragma unroll
+          for (int m = 0; m < NMW; ++m) {
+            if (!has[m]) continue;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (16 * (k0 + g) < rows) tmem_ld_x16(tbase + m * NMAX + 16 * (k0 + g), r[m][g]);
+          }
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
+          for (int m = 0; m < NMW; ++m) {
+            if (!has[m]) continue;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+              if (16 * (k0 + g) < rows) tmem_ld_ready(r[m][g]);
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const int k = k0 + g;
+            if (16 * k >= rows) break;
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = 0.f;
+#pragma unroll
+            for (int m = 0; m < NMW; ++m) {
+              if (!has[m]) continue;
+#pragma unroll
+              for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[m][g][c]);
+            }
+            if constexpr (FC1)
+              epilogue_chunk_fc1(p, v, lane, q, rb, start, rows, 16 * k, gsc);
+            else
+              epilogue_chunk_small<false>(p, v, lane, q, rb, start, rows, 16 * k, gsc);
+          }
         }
-        epilogue_chunk<FC1>(p, v, lane, q, rb, start, rows, c0, gsc);
       }
       tc_fence_before();
       __syncwarp();
@@ -465,14 +514,17 @@ int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
 // decode : tiles <= 16 pairs, steps of 2 weight blocks (256 of K), 9 steps in flight
 //          (162 KB), 3 slots, 3 MMA warps x 2 accumulator buffers, 3 dequant groups, pair
 //          rows as one 3-D box per step
-// prefill: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair rows each),
-//          1 MMA warp, 1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 16 rows
+// prefill: one SM per tile: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair
+//          rows each),
+//          1 MMA warp, 1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 64 rows
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
   if (sched == QMOE_SCHED_DECODE)
     return fc1 ? run<16, 9, 3, 2, 3, 3, 2, true, true>(tmap_b, p, num_sms, stream)
                : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, num_sms, stream);
+  if (sched == QMOE_SCHED_PREFILL_PAIR && p.nrb % 2 == 0 && num_sms >= 2)
+    return launch_gemm2(kind, tmap_b, p, num_sms, stream);
   return fc1 ? run<256, 8, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
              : run<256, 8, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
 }

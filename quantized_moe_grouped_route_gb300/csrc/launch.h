@@ -48,6 +48,10 @@ enum class GemmKind { kFc1, kFc2 };
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream);
 int gemm_tile_n(int sched);  // max pairs per tile for a schedule
+// Prefill GEMM on CTA pairs (two SMs per M = 256 tile, gemm2.cu); needs an even number
+// of 128-row weight blocks (p.nrb).
+cudaError_t launch_gemm2(GemmKind kind, const CUtensorMap& tmap_b, const GemmParams& p, int num_sms,
+                         cudaStream_t stream);
 // Rows and 64-wide slabs of the pair-row box the GEMM of a schedule loads: a 3-D box
 // {64 elements, rows, slabs} per pipeline step, or (slabs 0) 2-D boxes of rows x 64
 // elements.

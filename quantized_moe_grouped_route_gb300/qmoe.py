@@ -31,6 +31,7 @@ QMOE_FLAG_TIMEOUT = 2
 QMOE_SCHED_AUTO = 0
 QMOE_SCHED_DECODE = 1
 QMOE_SCHED_PREFILL = 2
+QMOE_SCHED_PREFILL_PAIR = 3
 QMOE_W13 = 1
 QMOE_W2 = 2
 
@@ -157,6 +158,8 @@ def workspace_views(ws: torch.Tensor, M, H, I, E, top_k, sched=QMOE_SCHED_AUTO) 
         "offsets": view(L["offsets"], E + 1, torch.int32),
         "sorted_pair": view(L["sorted_pair"], P, torch.int32),
         "pair_pos": view(L["pair_pos"], P, torch.int32),
+        "tiles": view(L["tiles"], 3 * qmoe_max_tiles(M, top_k, E, qmoe_sched_tile_n(sched, M, top_k, E)),
+                      torch.int32).view(-1, 3),
         "n_tiles": view(L["n_tiles"], 1, torch.int32),
         "xs": view(L["xs"], rows * H, torch.bfloat16).view(rows, H),
         "h": view(L["h"], rows * I, torch.bfloat16).view(rows, I),

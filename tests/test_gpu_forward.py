@@ -13,7 +13,8 @@ from tests.helpers import check_layer, gpu_forward
 
 pytestmark = pytest.mark.gpu
 
-SCHEDS = [qmoe.QMOE_SCHED_DECODE, qmoe.QMOE_SCHED_PREFILL, qmoe.QMOE_SCHED_AUTO]
+SCHEDS = [qmoe.QMOE_SCHED_DECODE, qmoe.QMOE_SCHED_PREFILL, qmoe.QMOE_SCHED_PREFILL_PAIR,
+          qmoe.QMOE_SCHED_AUTO]
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
@@ -33,7 +34,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s[0])
-@pytest.mark.parametrize("sched", SCHEDS[:2])
+@pytest.mark.parametrize("sched", SCHEDS[:3])
 def test_small_shapes_all_tokens(shape, sched):
     name, M, H, I, E, k = shape
     li = make_inputs(LayerConfig(name, M, H, I, E, k, seed=17), "cpu").to("cuda")
