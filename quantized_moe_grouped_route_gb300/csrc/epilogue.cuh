@@ -50,6 +50,31 @@ __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const fl
   }
 }
 
+// FC2 chunk with the tile's pair ids and scaled routing weights staged in shared
+// memory by the same warp (st_pair / st_w, indexed by column): no global load on the
+// chunk's path.
+__device__ __forceinline__ void epilogue_chunk_fc2_staged(const GemmParams& p, const float (&v)[16],
+                                                          int lane, int q, int rb, int rows,
+                                                          int c0, const int* st_pair,
+                                                          const float* st_w) {
+  const int jrow = rb * 128 + q * 32 + lane;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    if (c0 + c < rows) p.ypart[(size_t)st_pair[c0 + c] * p.H + jrow] = v[c] * st_w[c0 + c];
+  }
+}
+
+// Stage a tile's pair ids and routing weights x gsc for epilogue_chunk_fc2_staged (one
+// warp; the caller synchronises the warp before reading them back).
+__device__ __forceinline__ void epilogue_stage_fc2(const GemmParams& p, int lane, int start, int rows,
+                                                   float gsc, int* st_pair, float* st_w) {
+  for (int j = lane; j < rows; j += 32) {
+    const int pr = p.sorted_pair[start + j];
+    st_pair[j] = pr;
+    st_w[j] = p.topk_w[pr] * gsc;
+  }
+}
+
 // Chunk epilogue that reads the chunk's pair ids and routing weights itself (FC2) and
 // forms the SiLU with expf and an IEEE division (FC1).  The decode schedule uses it for
 // both GEMMs (there the epilogue overlaps the next unit's MMAs, and this form kept the

@@ -94,7 +94,10 @@ struct Cfg {
   static constexpr int kStageBytes = KS * kRawBytes;  // [KS codes blocks][KS scale blocks]
   static constexpr int kSlotCols = 64 * KS;
   static constexpr int kAccCol0 = SL * kSlotCols;  // TMEM: [A slots][acc: ACCB x NMW x NMAX]
-  static constexpr int kSmemBytes = SL * kBBytes + RS * kStageBytes + 1024 + kCtrlBytes;
+  // FC2 epilogue staging on the prefill schedule: per epilogue warp, a tile's pair ids
+  // and weights
+  static constexpr int kEpiBytes = NMW == 1 ? 4 * NMAX * 8 : 0;
+  static constexpr int kSmemBytes = SL * kBBytes + RS * kStageBytes + 1024 + kCtrlBytes + kEpiBytes;
   static constexpr int kThreads = gemm_threads(DG);
   static_assert(KS == 1 || KS == 2, "weight blocks per step");
   static_assert(kBBytes % 1024 == 0 && kStageBytes % 1024 == 0, "1024-byte stage alignment");
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* scale_lut = reinterpret_cast<uint32_t*>(ctrl + 1024);  // [256]
+  uint8_t* epi_stage = ctrl + kCtrlBytes;                          // [4][NMAX] ids, weights
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -412,6 +416,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
       const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
+      int* st_pair = reinterpret_cast<int*>(epi_stage + q * NMAX * 8);
+      float* st_w = reinterpret_cast<float*>(st_pair + NMAX);
+      if constexpr (!FC1 && !BIN) {
+        epilogue_stage_fc2(p, lane, start, rows, gsc, st_pair, st_w);
+        __syncwarp();
+      }
       if (!warp_wait(smem_u32(&accf[ab]), (local / ACCB) & 1, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t tbase =
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
             if constexpr (FC1)
               epilogue_chunk_fc1(p, v, lane, q, rb, start, rows, 16 * k, gsc);
             else
-              epilogue_chunk_small<false>(p, v, lane, q, rb, start, rows, 16 * k, gsc);
+              epilogue_chunk_fc2_staged(p, v, lane, q, rb, rows, 16 * k, st_pair, st_w);
           }
         }
       }
