@@ -200,6 +200,18 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic launch
+// The forward's kernels after route are launched with programmatic stream
+// serialization: a kernel may start while its predecessor finishes.  grid_dep_wait()
+// blocks the calling thread until the predecessor grid has completed and its memory is
+// visible (a no-op for a launch without the attribute); a thread must call it before
+// it reads anything the predecessor writes.  grid_dep_launch() lets the successor be
+// scheduled (as soon as every CTA of this grid has called it or exited).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     tmem_relinquish();
   }
   if (warp == (BIN ? kMmaWarp0 : kPairTmaWarp) && lane == 0) prefetch_tmap(&tmap_b);
+  grid_dep_launch();  // the next kernel may take SMs as this grid's CTAs finish
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // ------------------------------------------------------------ pair-row TMA producer
     const uint32_t leader = elect_one();
     const uint64_t pol = l2_policy_evict_last();
+    grid_dep_wait();  // the pair rows are the previous kernel's output
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -286,7 +288,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       bks += NMW;
       return true;
     };
-    if constexpr (BIN) ok = issue_b();
+    if constexpr (BIN) {
+      grid_dep_wait();  // the pair rows are the previous kernel's output
+      ok = issue_b();
+    }
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
       const int t = u / p.nrb;
       const int rows = p.tiles[3 * t + 2];
@@ -509,8 +514,15 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
   auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, KS, BIN, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
-  k<<<num_sms, C::kThreads, C::kSmemBytes, stream>>>(tmap, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, tmap, p);
 }
 
 }  // namespace

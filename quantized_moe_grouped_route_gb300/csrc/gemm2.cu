@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
     tmem_relinquish2();
   }
   if (warp == kPairWarp && lane == 0) prefetch_tmap(&tmap_b);
+  grid_dep_launch();
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer's barriers exist before any remote arrival
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
     // this CTA's half of the tile's rows: columns rank*N/2 .. of the MMA's N
     const uint32_t lead = elect_one();
     const uint64_t pol = l2_policy_evict_last();
+    grid_dep_wait();  // the pair rows are the previous kernel's output
     uint32_t it = 0;
     bool ok = true;
     for (int u = cl; u < n_units && ok; u += ncl) {
@@ -467,16 +469,17 @@ cudaError_t run2(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cuda
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // one CTA pair per pair of SMs that can hold it
   cfg.gridDim = dim3((unsigned)(num_sms & ~1));
   int clusters = 0;

@@ -44,6 +44,15 @@ struct GemmParams {
   unsigned int* err;
 };
 
+// Launch attribute that lets a kernel start while the previous kernel on the stream
+// finishes (it must then call grid_dep_wait before reading that kernel's outputs).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 enum class GemmKind { kFc1, kFc2 };
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream);

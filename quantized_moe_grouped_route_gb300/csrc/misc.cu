@@ -57,6 +57,8 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N
 __global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pair,
                               const int32_t* __restrict__ n_valid_p, int top_k, int chunks,
                               uint4* __restrict__ xs) {
+  grid_dep_wait();    // the route's outputs
+  grid_dep_launch();  // FC1 may start streaming weights
   const long long total = (long long)(*n_valid_p) * chunks;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -72,6 +74,7 @@ __global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __rest
 // atomics: deterministic.  8 columns per thread.
 __global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ ids,
                                int M, int top_k, int E, int H, uint4* __restrict__ out) {
+  grid_dep_wait();  // FC2's partial rows
   const int c8 = H / 8;
   const long long total = (long long)M * c8;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -166,18 +169,29 @@ cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int 
 cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
                           int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream) {
   const int chunks = H / 8;
-  gather_kernel<<<grid_for((long long)P * chunks, 256, num_sms), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(x), sorted_pair, n_valid, top_k, chunks,
-      reinterpret_cast<uint4*>(xs));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3(grid_for((long long)P * chunks, 256, num_sms));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_kernel, reinterpret_cast<const uint4*>(x), sorted_pair,
+                            n_valid, top_k, chunks, reinterpret_cast<uint4*>(xs));
 }
 
 cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
                            void* out, int num_sms, cudaStream_t stream) {
   const long long work = (long long)M * (H / 8);
-  combine_kernel<<<grid_for(work, 256, num_sms), 256, 0, stream>>>(
-      ypart, ids, M, top_k, E, H, reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.gridDim = dim3(grid_for(work, 256, num_sms));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, ypart, ids, M, top_k, E, H,
+                            reinterpret_cast<uint4*>(out));
 }
 
 cudaError_t launch_selftest_dequant(uint16_t* out, cudaStream_t stream) {
