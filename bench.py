@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 DEFAULT_CONFIG = "decode_m16_h7168_i2048_e256_k8"
 METRIC = "MoE layer tokens/s (decode M=16, H=7168, I=2048, E=256, top_k=8, NVFP4 W4A16)"
 STAGES = ["route", "gather", "fc1", "fc2", "combine"]
-KERNEL_SOURCES = ["csrc/gemm.cu", "csrc/dequant.cuh", "csrc/common.cuh"]
+KERNEL_SOURCES = ["csrc/gemm.cu", "csrc/dequant.cuh", "csrc/common.cuh", "csrc/epilogue.cuh"]
 
 
 def parse():
