@@ -33,7 +33,11 @@ __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const fl
   // forms h(i, c) and lane j + 16 forms h(i, c+1): every lane computes and stores.
   const bool is_up = lane < 16;
   const int i = rb * 64 + q * 16 + (lane & 15);
-  __nv_bfloat16* hp = reinterpret_cast<__nv_bfloat16*>(p.h);
+  // every operand read before the first store: a store through a plain pointer could
+  // alias anything read through one afterwards, which would serialise each store
+  // behind a reload
+  __nv_bfloat16* const hp = reinterpret_cast<__nv_bfloat16*>(p.h);
+  const size_t I = (size_t)p.I;
   float hv[8];
 #pragma unroll
   for (int c = 0; c < 16; c += 2) {
@@ -46,7 +50,7 @@ __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const fl
 #pragma unroll
   for (int c = 0; c < 16; c += 2) {
     const int col = c0 + c + (is_up ? 0 : 1);
-    if (col < rows) hp[(size_t)(start + col) * p.I + i] = __float2bfloat16_rn(hv[c >> 1]);
+    if (col < rows) hp[(size_t)(start + col) * I + i] = __float2bfloat16_rn(hv[c >> 1]);
   }
 }
 
@@ -58,9 +62,19 @@ __device__ __forceinline__ void epilogue_chunk_fc2_staged(const GemmParams& p, c
                                                           int c0, const int* st_pair,
                                                           const float* st_w) {
   const int jrow = rb * 128 + q * 32 + lane;
+  // every operand read before the first store (see epilogue_chunk_fc1)
+  float* const yp = p.ypart;
+  const size_t H = (size_t)p.H;
+  int pr[16];
+  float w[16];
+#pragma unroll
+  for (int c = 0; c < 16; c += 4) {
+    *reinterpret_cast<int4*>(pr + c) = *reinterpret_cast<const int4*>(st_pair + c0 + c);
+    *reinterpret_cast<float4*>(w + c) = *reinterpret_cast<const float4*>(st_w + c0 + c);
+  }
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
-    if (c0 + c < rows) p.ypart[(size_t)st_pair[c0 + c] * p.H + jrow] = v[c] * st_w[c0 + c];
+    if (c0 + c < rows) yp[(size_t)pr[c] * H + jrow] = v[c] * w[c];
   }
 }
 
