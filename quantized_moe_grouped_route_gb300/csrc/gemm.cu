@@ -11,14 +11,15 @@
 // batches still fill the instruction, and every output element is produced by one
 // CTA in a fixed order (deterministic, no split reduction).
 //
-// Data path per 128-wide K step (one pipeline step):
-//   TMA warps     : bulk copy of the step's packed codes (8 KB) and scales (1 KB)
-//                   into the weight ring; tiled TMA of the pair rows (bf16, 128-byte
-//                   swizzle) into the pair-row ring
+// Data path per pipeline step (KS x 128 of K):
+//   weight TMA    : bulk copies of the step's packed codes (8 KB per block) and scales
+//                   (1 KB per block) into the weight ring
+//   pair rows     : tiled TMA of the tile's gathered activations (bf16, 128-byte
+//                   swizzle) into the slot's shared-memory stage
 //   dequant warps : codes -> bf16 in registers (bit placement + one bf16x2 multiply
 //                   by the block scale) -> tcgen05.st into TMEM (the MMA's A operand)
-//   MMA warp      : 8 x tcgen05.mma kind::f16, A from TMEM, B from smem, fp32
-//                   accumulator in TMEM; commits release the stage
+//   MMA warp(s)   : 8 x tcgen05.mma kind::f16 per block, A from TMEM, B from smem,
+//                   fp32 accumulator in TMEM; commits release the slot
 //   epilogue warps: tcgen05.ld of the accumulator, scale, SwiGLU or routing weight,
 //                   global stores
 // The dequantized weights never touch shared memory, which leaves the smem
