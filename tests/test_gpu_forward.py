@@ -91,3 +91,19 @@ def test_zero_tokens_is_a_noop():
     w = torch.empty(0, 2, dtype=torch.float32, device="cuda")
     out = layer(x, ids, w)
     assert out.shape == (0, li.cfg.H)
+
+
+@pytest.mark.parametrize("cfg", [c for c in CONFIGS if c.name.startswith("prefill")],
+                         ids=lambda c: c.name)
+def test_prefill_pair_schedule_is_bit_identical(cfg):
+    """The two-SM prefill GEMM accumulates each output in the same K order as the
+    one-SM kernel (whose results the oracle checks above), so the two schedules must
+    agree bit for bit on the full workloads; each is also run-to-run deterministic."""
+    li = make_inputs(cfg, "cuda")
+    layer = qmoe.NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
+    outs = [layer(li.x, li.topk_ids, li.topk_weights, sched=s).view(torch.int16).clone()
+            for s in (qmoe.QMOE_SCHED_PREFILL, qmoe.QMOE_SCHED_PREFILL_PAIR,
+                      qmoe.QMOE_SCHED_PREFILL_PAIR)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[1], outs[2]), "two-SM schedule not deterministic"
+    assert torch.equal(outs[0], outs[1]), "two-SM and one-SM schedules differ"
