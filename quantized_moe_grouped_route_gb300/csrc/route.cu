@@ -22,6 +22,7 @@ namespace qmoe {
 namespace {
 
 constexpr int kWarps = kRouteThreads / 32;
+constexpr int kBatch = 8;  // 32-pair steps whose ids a warp loads at once
 
 // Block-wide exclusive scan of one int per thread; returns the exclusive prefix and
 // writes the block total to *total.  `scratch` holds kWarps ints.
@@ -70,21 +71,27 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   int* hw = hist + w * E;
   bool bad = false;
 
-  // A. warp-aggregated histogram
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    int e = -1;
-    if (i < hi) {
-      e = ids[i];
+  // A. warp-aggregated histogram.  The ids of kBatch steps are loaded before the
+  // first is used, so a warp waits for global memory once per batch, not per step.
+  for (int base0 = lo; base0 < hi; base0 += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = base0 + 32 * k + lane;
+      eb[k] = i < hi ? ids[i] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      int e = eb[k];
       if (e >= E) {
         bad = true;
         e = -1;
       }
       if (e < 0) e = -1;
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(m) - 1) hw[e] += __popc(m);
+      __syncwarp();
     }
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(m) - 1) hw[e] += __popc(m);
-    __syncwarp();
   }
   if (bad) atomicOr(err, QMOE_FLAG_BAD_ID);
   __syncthreads();
@@ -132,27 +139,33 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncthreads();
 
-  // C. stable scatter
+  // C. stable scatter (steps in order within each batch, batches in order)
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    int e = -1;
-    if (i < hi) {
-      e = ids[i];
-      if (e >= E || e < 0) e = -1;
+  for (int base0 = lo; base0 < hi; base0 += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = base0 + 32 * k + lane;
+      eb[k] = i < hi ? ids[i] : -1;
     }
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    const int b = e >= 0 ? hw[e] : 0;
-    const int pos = b + __popc(m & lt_mask);
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(m) - 1) hw[e] = b + __popc(m);
-    __syncwarp();
-    if (i < hi) {
-      if (e >= 0) {
-        sorted_pair[pos] = i;
-        pair_pos[i] = pos;
-      } else {
-        pair_pos[i] = -1;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = base0 + 32 * k + lane;
+      int e = eb[k];
+      if (e >= E || e < 0) e = -1;
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      const int b = e >= 0 ? hw[e] : 0;
+      const int pos = b + __popc(m & lt_mask);
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(m) - 1) hw[e] = b + __popc(m);
+      __syncwarp();
+      if (i < hi) {
+        if (e >= 0) {
+          sorted_pair[pos] = i;
+          pair_pos[i] = pos;
+        } else {
+          pair_pos[i] = -1;
+        }
       }
     }
   }
