@@ -53,19 +53,28 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N
   }
 }
 
-// xs[pos] = x[sorted_pair[pos] / top_k] for the n_valid routed pairs (16-byte chunks).
+// xs[pos] = x[sorted_pair[pos] / top_k] for the n_valid routed pairs, 16-byte chunks.
+// Work items are (row, segment of 256 chunks) taken one per warp: the row's source is
+// looked up once per item, and small batches still spread over many warps.
 __global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pair,
                               const int32_t* __restrict__ n_valid_p, int top_k, int chunks,
                               uint4* __restrict__ xs) {
   grid_dep_wait();    // the route's outputs
   grid_dep_launch();  // FC1 may start streaming weights
-  const long long total = (long long)(*n_valid_p) * chunks;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const int pos = (int)(idx / chunks);
-    const int c = (int)(idx - (long long)pos * chunks);
+  constexpr int kSeg = 256;
+  const int nseg = (chunks + kSeg - 1) / kSeg;
+  const long long items = (long long)(*n_valid_p) * nseg;
+  const int lane = threadIdx.x & 31;
+  const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long it = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items;
+       it += warps) {
+    const int pos = (int)(it / nseg);
+    const int c0 = (int)(it - (long long)pos * nseg) * kSeg;
+    const int c1 = min(chunks, c0 + kSeg);
     const int tok = sorted_pair[pos] / top_k;
-    xs[idx] = x[(size_t)tok * chunks + c];
+    const uint4* src = x + (size_t)tok * chunks;
+    uint4* dst = xs + (size_t)pos * chunks;
+    for (int c = c0 + lane; c < c1; c += 32) dst[c] = src[c];
   }
 }
 
@@ -171,7 +180,8 @@ cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32
   const int chunks = H / 8;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  cfg.gridDim = dim3(grid_for((long long)P * chunks, 256, num_sms));
+  // a warp per (row, 256-chunk segment)
+  cfg.gridDim = dim3(grid_for((long long)P * ((chunks + 255) / 256) * 32, 256, num_sms));
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cfg.attrs = attr;
