@@ -50,7 +50,7 @@ extern "C" {
 /* Tile schedules for moe_nvfp4_forward. */
 #define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
 #define QMOE_SCHED_DECODE 1  /* tiles of <= 16 pairs: weight streaming, HBM bound */
-#define QMOE_SCHED_PREFILL 2 /* tiles of <= 256 pairs: tensor bound */
+#define QMOE_SCHED_PREFILL 2 /* tiles of <= 320 pairs: tensor bound */
 /* As PREFILL, with each 256-row weight tile on a pair of SMs (tcgen05 2-CTA MMAs, each
    SM holding half of the tile's pair rows); a GEMM whose count of 128-row weight blocks
    is odd runs as PREFILL.  Same results as PREFILL; slower than it at present. */

@@ -292,6 +292,48 @@ __device__ __forceinline__ void mma_bf16_ts_step8(uint32_t pred, uint32_t d_tmem
       : "memory");
 }
 
+// The 4 MMAs of one 64-wide K slab: D (+)= A[a_tmem + 8j] * B[desc + 2j], j = 0..3.
+// Only the first can start a fresh accumulation.
+__device__ __forceinline__ void mma_bf16_ts_slab4(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint32_t desc_lo, uint32_t desc_hi,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q, t;\n\t.reg .b64 d;\n\t.reg .b32 lo, a;\n\t"
+      "setp.ne.b32 p, %0, 0;\n\t"
+      "setp.ne.b32 q, %6, 0;\n\t"
+      "setp.eq.u32 t, 0, 0;\n\t"
+      "mov.b64 d, {%3, %4};\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], d, %5, q;\n\t"
+      "add.u32 lo, %3, 2;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 8;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %5, t;\n\t"
+      "add.u32 lo, %3, 4;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 16;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %5, t;\n\t"
+      "add.u32 lo, %3, 6;\n\tmov.b64 d, {lo, %4};\n\tadd.u32 a, %2, 24;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [a], d, %5, t;\n\t}" ::"r"(pred),
+      "r"(d_tmem), "r"(a_tmem), "r"(desc_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// As mma_bf16_ts_slab4 into two accumulators of one tile wider than 256 pairs: chain 0
+// takes B rows 0..255 into d0, chain 1 the rows from 256 on (`off16` 16-byte units
+// further on) into d1, alternating slice by slice so that each MMA of the narrow
+// chain issues behind an independent one and its accumulation latency stays hidden.
+__device__ __forceinline__ void mma_bf16_ts_slab4x2(uint32_t pred, uint32_t d0, uint32_t d1,
+                                                    uint32_t a_tmem, uint32_t desc_lo,
+                                                    uint32_t desc_hi, uint32_t off16,
+                                                    uint32_t idesc0, uint32_t idesc1,
+                                                    uint32_t accumulate) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = desc_lo + 2u * j;
+    const uint64_t b0 = ((uint64_t)desc_hi << 32) | lo;
+    const uint64_t b1 = ((uint64_t)desc_hi << 32) | (lo + off16);
+    const uint32_t acc = j == 0 ? accumulate : 1u;
+    mma_bf16_ts_if(pred, d0, a_tmem + 8u * j, b0, idesc0, acc);
+    mma_bf16_ts_if(pred, d1, a_tmem + 8u * j, b1, idesc1, acc);
+  }
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (bf16 inputs, fp32 accumulate).
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {

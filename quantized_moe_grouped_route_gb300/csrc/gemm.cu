@@ -82,8 +82,12 @@ __host__ __device__ constexpr int gemm_threads(int groups) { return (kDequantWar
 // Pair rows: with BIN the tile's rows of one K step (both 64-wide slabs) arrive in a
 // single 3-D box copy {64 elements, NMAX rows, 2 slabs}, issued by the MMA warp that
 // owns the step; otherwise a producer warp copies 2-D boxes of kPairBoxRows rows x 64
-// elements, as many as the tile needs.  One copy per step, from warps spread over the
-// schedulers, keeps copy issue off the path that feeds the MMA.
+// elements, as many as the tile needs, slab by slab: a slot's slab 0 is refilled as
+// soon as the MMAs of the previous step that read it have completed (their own
+// commit), and slab 1 lands on its own barrier, which gives the copies (up to 80 KB a
+// step, more time than the step's MMAs take at the rate the pair rows arrive) half a
+// step more lead than whole-slot refills.  One copy per step, from warps spread over
+// the schedulers, keeps copy issue off the path that feeds the MMA.
 // A pipeline step covers KS weight blocks (KS x 128 of K): KS x 9 KB of the weight ring,
 // a TMEM A slot of KS x 64 columns, 2 KS slabs of pair rows and 8 KS MMAs, so the
 // per-step barrier and bookkeeping work is paid once per KS blocks.  The last step of
@@ -103,12 +107,14 @@ struct Cfg {
   static_assert(KS == 1 || KS == 2, "weight blocks per step");
   static_assert(kBBytes % 1024 == 0 && kStageBytes % 1024 == 0, "1024-byte stage alignment");
   static_assert(SL * kSlotCols + ACCB * NMW * NMAX <= kTmemCols, "TMEM budget");
-  static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "MMA N range");
+  // a tile wider than one MMA's N (256) takes two accumulator chains (256 + the rest)
+  static_assert(NMAX % 16 == 0 && NMAX >= 16 && (NMAX <= 256 || (NMAX <= 512 && NMW == 1)),
+                "MMA N range");
   static_assert(NMW >= 1 && NMW <= 3, "MMA warps 1..3");
   static_assert(SL % DG == 0 && SL % NMW == 0, "each slot needs one dequant group and one MMA warp");
   static_assert(RS % DG == 0, "each weight stage needs one dequant group");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert((2 * RS + SL * (KS + 1) + 2 * ACCB + 1) * 8 + 16 <= 1024, "barrier area");
+  static_assert((2 * RS + SL * (KS + 3) + 2 * ACCB + 1) * 8 + 16 <= 1024, "barrier area");
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -144,7 +150,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   uint64_t* accf = sempty + SL;                         // accumulators ready (NMW commits)
   uint64_t* acce = accf + ACCB;                         // accumulators drained (4 warps)
   uint64_t* drain = acce + ACCB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // 2-D pair-row boxes (no BIN): slab 0 of a slot may be refilled once the previous
+  // step's slab-0 MMAs have completed (bempty0), slab 1 lands on its own barrier
+  // (bfull1), so the copy of a slot's first slab starts half a step earlier
+  uint64_t* bempty0 = drain + 1;
+  uint64_t* bfull1 = bempty0 + SL;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfull1 + SL);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* scale_lut = reinterpret_cast<uint32_t*>(ctrl + 1024);  // [256]
   uint8_t* epi_stage = ctrl + kCtrlBytes;                          // [4][NMAX] ids, weights
@@ -164,6 +175,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       mbar_init(smem_u32(&acce[a]), 4);
     }
     mbar_init(smem_u32(drain), NMW);
+    for (int s = 0; s < SL; ++s) {
+      mbar_init(smem_u32(&bempty0[s]), 1);
+      mbar_init(smem_u32(&bfull1[s]), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -229,21 +244,26 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const int t = u / p.nrb;
       const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int nbox = (rows + kPairBoxRows - 1) / kPairBoxRows;
-      const uint32_t tx = 2u * (uint32_t)nbox * (uint32_t)(kPairBoxRows * 128);
-      for (int ks = 0; ks < nks; ++ks, ++it) {
+      const uint32_t tx = (uint32_t)nbox * (uint32_t)(kPairBoxRows * 128);  // one slab
+      for (int ks = 0; ks < nks && ok; ++ks, ++it) {
         const int s = it % SL;
-        if (!warp_wait(smem_u32(&sempty[s]), ((it / SL) & 1) ^ 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
+        const uint32_t eph = ((it / SL) & 1) ^ 1;
         const uint32_t st = smem_u32(bring + s * C::kBBytes);
-        const uint32_t fb = smem_u32(&sfull[s * KS]);
-        mbar_arrive_expect_tx_if(leader, fb, tx);
 #pragma unroll
-        for (int sl = 0; sl < 2; ++sl)
+        for (int sl = 0; sl < 2; ++sl) {
+          // slab 0 is free once the slot's previous slab-0 MMAs completed, slab 1 once
+          // the whole previous step did
+          const uint32_t eb = smem_u32(sl == 0 ? &bempty0[s] : &sempty[s]);
+          if (!warp_wait(eb, eph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(sl == 0 ? &sfull[s * KS] : &bfull1[s]);
+          mbar_arrive_expect_tx_if(leader, fb, tx);
           for (int g = 0; g < nbox; ++g)
             tma_load_2d_if(leader, st + sl * C::kBSlab + g * kPairBoxRows * 128, &tmap_b,
                            ks * kBK + sl * 64, start + g * kPairBoxRows, fb, pol);
+        }
       }
     }
     if (!ok) {  // the pair rows of the last slots may still be landing
@@ -258,6 +278,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     const int m = warp - kMmaWarp0;
     const uint32_t leader = elect_one();
     const uint32_t sfull_u = smem_u32(&sfull[0]), sempty_u = smem_u32(&sempty[0]);
+    const uint32_t bempty0_u = smem_u32(&bempty0[0]), bfull1_u = smem_u32(&bfull1[0]);
     const uint64_t bdesc0 = sdesc_sw128(smem_u32(bring));
     const uint32_t bdesc_lo0 = (uint32_t)bdesc0, bdesc_hi = (uint32_t)(bdesc0 >> 32);
     uint32_t it = 0, local = 0;
@@ -296,7 +317,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
       const int t = u / p.nrb;
       const int rows = p.tiles[3 * t + 2];
-      const uint32_t idesc = idesc_bf16_f32(128, ((rows + 15) >> 4) << 4);
+      const int n16 = ((rows + 15) >> 4) << 4;
+      const uint32_t idesc = idesc_bf16_f32(128, n16 < 256 ? n16 : 256);
+      // tiles wider than 256 pairs: a second chain over the rest (NMAX > 256 only)
+      const uint32_t idesc2 = idesc_bf16_f32(128, n16 > 256 ? n16 - 256 : 16);
       const int ab = local % ACCB;
       if (!warp_wait(smem_u32(&acce[ab]), ((local / ACCB) & 1) ^ 1, abort_flag, p.err)) {
         ok = false;
@@ -315,9 +339,34 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           break;
         }
         tc_fence_after();
-        mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols,
-                          bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4, idesc,
-                          ks != ks0 ? 1u : 0u);
+        if constexpr (!BIN) {
+          // slab by slab: the first slab's stage is released (bempty0) as soon as its
+          // MMAs complete, the second may still be landing (bfull1)
+          const uint32_t a0 = tmem + sl * C::kSlotCols;
+          const uint32_t b0 = bdesc_lo0 + sl * (C::kBBytes >> 4);
+          const uint32_t acc = ks != ks0 ? 1u : 0u;
+          if (NMAX > 256 && n16 > 256)
+            mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0, b0, bdesc_hi, (256 * 128) >> 4,
+                                idesc, idesc2, acc);
+          else
+            mma_bf16_ts_slab4(leader, d_tmem, a0, b0, bdesc_hi, idesc, acc);
+          tc_commit_if(leader, bempty0_u + sl * 8);
+          if (!warp_wait(bfull1_u + sl * 8, sph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b1 = b0 + (C::kBSlab >> 4);
+          if (NMAX > 256 && n16 > 256)
+            mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0 + 32, b1, bdesc_hi,
+                                (256 * 128) >> 4, idesc, idesc2, 1u);
+          else
+            mma_bf16_ts_slab4(leader, d_tmem, a0 + 32, b1, bdesc_hi, idesc, 1u);
+        } else {
+          mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols,
+                            bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4, idesc,
+                            ks != ks0 ? 1u : 0u);
+        }
         if (KS == 2 && (ks != nks - 1 || last_halves == 2)) {
           if (!warp_wait(sfull_u + (sl * KS + 1) * 8, sph, abort_flag, p.err)) {
             ok = false;
@@ -528,7 +577,9 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 
 }  // namespace
 
-int gemm_tile_n(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : 256; }
+int gemm_tile_n(int sched) {
+  return sched == QMOE_SCHED_DECODE ? 16 : sched == QMOE_SCHED_PREFILL_PAIR ? 256 : 320;
+}
 
 int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : kPairBoxRows; }
 
@@ -537,9 +588,11 @@ int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
 // decode : tiles <= 16 pairs, steps of 2 weight blocks (256 of K), 9 steps in flight
 //          (162 KB), 3 slots, 3 MMA warps x 2 accumulator buffers, 3 dequant groups, pair
 //          rows as one 3-D box per step
-// prefill: one SM per tile: tiles <= 256 pairs, 8 weight steps, 2 slots (64 KB of pair
-//          rows each),
-//          1 MMA warp, 1 accumulator (256 columns), 2 dequant groups, 2-D boxes of 64 rows
+// prefill: one SM per tile: tiles <= 320 pairs (an expert of up to 320 routed pairs is
+//          one tile, so its weights are dequantized once per row block), 6 weight
+//          steps, 2 slots (80 KB of pair rows each), 1 MMA warp, 1 accumulator (320
+//          columns: MMAs of N = 256 and of the rest), 2 dequant groups, 2-D boxes of
+//          64 rows
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
@@ -548,8 +601,8 @@ cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, con
                : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, num_sms, stream);
   if (sched == QMOE_SCHED_PREFILL_PAIR && p.nrb % 2 == 0 && num_sms >= 2)
     return launch_gemm2(kind, tmap_b, p, num_sms, stream);
-  return fc1 ? run<256, 8, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
-             : run<256, 8, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
+  return fc1 ? run<320, 6, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
+             : run<320, 6, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
 }
 
 }  // namespace qmoe

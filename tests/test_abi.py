@@ -27,7 +27,8 @@ def test_size_queries(lib):
     assert qmoe.qmoe_max_tiles(16, 8, 256, 32) == 4 + 256
     assert qmoe.qmoe_max_tiles(8192, 8, 256, 256) == 256 + 256
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 16, 8, 256) == 16
-    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 8192, 8, 256) == 256
+    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 8192, 8, 256) == 320
+    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_PREFILL_PAIR, 8192, 8, 256) == 256
     assert qmoe.qmoe_repacked_fp4_size(256, 4096, 7168) == 256 * 4096 * 3584
     assert qmoe.qmoe_repacked_scale_size(256, 7168, 2048) == 256 * 7168 * 128
     ws = qmoe.qmoe_forward_workspace_size(8192, 7168, 2048, 256, 8)

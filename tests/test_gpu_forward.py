@@ -30,6 +30,9 @@ SMALL = [
     ("m300_h384_i128_e3_k2", 300, 384, 128, 3, 2),
     ("m70_h128_i384_e1_k1", 70, 128, 384, 1, 1),
     ("m129_h512_i256_e16_k4", 129, 512, 256, 16, 4),
+    # experts of 257..320 pairs (one two-chain prefill tile) and of more (a tail tile)
+    ("m580_h256_i128_e2_k1", 580, 256, 128, 2, 1),
+    ("m700_h256_i256_e2_k1", 700, 256, 256, 2, 1),
 ]
 
 

@@ -93,7 +93,7 @@ def _check_route(ids: torch.Tensor, E: int, tile_n: int):
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=lambda c: c.name)
-@pytest.mark.parametrize("tile_n", [32, 256])
+@pytest.mark.parametrize("tile_n", [16, 32, 256, 320])
 def test_route_configs_bit_exact(cfg, tile_n):
     g = torch.Generator(device="cuda").manual_seed(cfg.seed)
     ids, _ = _routing(cfg, g, "cuda")
