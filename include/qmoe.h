@@ -50,7 +50,9 @@ extern "C" {
 /* Tile schedules for moe_nvfp4_forward. */
 #define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
 #define QMOE_SCHED_DECODE 1  /* tiles of <= 16 pairs: weight streaming, HBM bound */
-#define QMOE_SCHED_PREFILL 2 /* tiles of <= 320 pairs: tensor bound */
+/* Tensor bound: tiles of <= 320 pairs when experts average >= 192 pairs, else tiles of
+   <= 192 pairs whose epilogue overlaps the next tile's MMAs. */
+#define QMOE_SCHED_PREFILL 2
 /* As PREFILL, with each 256-row weight tile on a pair of SMs (tcgen05 2-CTA MMAs, each
    SM holding half of the tile's pair rows); a GEMM whose count of 128-row weight blocks
    is odd runs as PREFILL.  Same results as PREFILL; slower than it at present. */

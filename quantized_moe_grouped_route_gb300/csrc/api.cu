@@ -89,10 +89,16 @@ int check_shape(int M, int H, int I, int E, int top_k) {
   return QMOE_OK;
 }
 
+// The schedule a call runs.  PREFILL takes one of two tile shapes by the mean count
+// of pairs per expert: from 192 on, tiles of up to 320 pairs with one accumulator (an
+// expert's rows in one tile, the weights dequantized once per row block, the widest
+// MMAs); below, tiles of up to 192 pairs with two accumulators, so that the epilogue
+// of a tile overlaps the MMAs of the next (small tiles are epilogue-heavy).
 int resolve_sched(int sched, int M, int top_k, int E) {
-  if (sched == QMOE_SCHED_DECODE || sched == QMOE_SCHED_PREFILL || sched == QMOE_SCHED_PREFILL_PAIR)
-    return sched;
-  return (long long)M * top_k <= 4LL * E ? QMOE_SCHED_DECODE : QMOE_SCHED_PREFILL;
+  const long long P = (long long)M * top_k;
+  if (sched == QMOE_SCHED_DECODE || sched == QMOE_SCHED_PREFILL_PAIR) return sched;
+  if (sched == QMOE_SCHED_AUTO && P <= 4LL * E) return QMOE_SCHED_DECODE;
+  return P >= 192LL * E ? QMOE_SCHED_PREFILL : kSchedPrefillNarrow;
 }
 
 ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {

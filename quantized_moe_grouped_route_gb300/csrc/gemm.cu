@@ -579,7 +579,9 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
 }  // namespace
 
 int gemm_tile_n(int sched) {
-  return sched == QMOE_SCHED_DECODE ? 16 : sched == QMOE_SCHED_PREFILL_PAIR ? 256 : 320;
+  if (sched == QMOE_SCHED_DECODE) return 16;
+  if (sched == QMOE_SCHED_PREFILL_PAIR) return 256;
+  return sched == kSchedPrefillNarrow ? 192 : 320;
 }
 
 int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : kPairBoxRows; }
@@ -593,7 +595,11 @@ int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
 //          one tile, so its weights are dequantized once per row block), 6 weight
 //          steps, 2 slots (80 KB of pair rows each), 1 MMA warp, 1 accumulator (320
 //          columns: MMAs of N = 256 and of the rest), 2 dequant groups, 2-D boxes of
-//          64 rows
+//          64 rows.  An MMA costs about the same for any N from about 160 to 256, so
+//          wide tiles make the most of the tensor cores, at the price of an epilogue
+//          that stalls the MMAs (one accumulator fills the TMEM);
+//          narrow variant (experts averaging < 192 pairs): tiles <= 192 pairs, 8
+//          weight steps, 2 accumulators, so the epilogue overlaps the next tile's MMAs
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
@@ -602,6 +608,9 @@ cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, con
                : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, num_sms, stream);
   if (sched == QMOE_SCHED_PREFILL_PAIR && p.nrb % 2 == 0 && num_sms >= 2)
     return launch_gemm2(kind, tmap_b, p, num_sms, stream);
+  if (sched == kSchedPrefillNarrow)
+    return fc1 ? run<192, 8, 2, 2, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
+               : run<192, 8, 2, 2, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
   return fc1 ? run<320, 6, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
              : run<320, 6, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
 }

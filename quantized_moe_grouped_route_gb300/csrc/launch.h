@@ -56,6 +56,9 @@ inline cudaLaunchAttribute pdl_attribute() {
 enum class GemmKind { kFc1, kFc2 };
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream);
+// Internal schedule: PREFILL with tiles of up to 192 pairs and two accumulators
+// (chosen for PREFILL when experts average fewer than 192 pairs).
+constexpr int kSchedPrefillNarrow = 16;
 int gemm_tile_n(int sched);  // max pairs per tile for a schedule
 // Prefill GEMM on CTA pairs (two SMs per M = 256 tile, gemm2.cu); needs an even number
 // of 128-row weight blocks (p.nrb).

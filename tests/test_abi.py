@@ -28,6 +28,9 @@ def test_size_queries(lib):
     assert qmoe.qmoe_max_tiles(8192, 8, 256, 256) == 256 + 256
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 16, 8, 256) == 16
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 8192, 8, 256) == 320
+    # experts averaging fewer than 192 pairs: the narrow prefill tiles
+    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 2048, 8, 128) == 192
+    assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_PREFILL, 16, 8, 256) == 192
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_PREFILL_PAIR, 8192, 8, 256) == 256
     assert qmoe.qmoe_repacked_fp4_size(256, 4096, 7168) == 256 * 4096 * 3584
     assert qmoe.qmoe_repacked_scale_size(256, 7168, 2048) == 256 * 7168 * 128
