@@ -54,6 +54,36 @@ __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const fl
   }
 }
 
+// epilogue_chunk_fc1 through a per-warp shared tile [16 pairs][16 intermediate indices]
+// bf16 (512 bytes): the h values go in as one 16-bit store each (the two half-warps
+// fill rows 32 bytes apart, no bank conflicts) and come out as 16-byte rows, so each
+// lane writes one 16-byte piece of a pair's h row: one global store per lane and
+// chunk instead of eight 2-byte ones (global store issue dominates this epilogue).
+__device__ __forceinline__ void epilogue_chunk_fc1_tr(const GemmParams& p, const float (&v)[16],
+                                                      int lane, int q, int rb, int start, int rows,
+                                                      int c0, float gsc, uint8_t* tile) {
+  const bool is_up = lane < 16;
+  float hv[8];
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const float send = (is_up ? v[c + 1] : v[c]) * gsc;
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    const float up = is_up ? v[c] * gsc : recv;
+    const float gate = is_up ? recv : v[c + 1] * gsc;
+    hv[c >> 1] = silu_mul(gate, up);
+  }
+  __nv_bfloat16* const t = reinterpret_cast<__nv_bfloat16*>(tile) + (lane & 15);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) t[(2 * m + (is_up ? 0 : 1)) * 16] = __float2bfloat16_rn(hv[m]);
+  __syncwarp();
+  const int col = lane >> 1, half = lane & 1;
+  const uint4 w = *reinterpret_cast<const uint4*>(tile + col * 32 + half * 16);
+  __nv_bfloat16* const hp = reinterpret_cast<__nv_bfloat16*>(p.h);
+  if (c0 + col < rows)
+    *reinterpret_cast<uint4*>(hp + (size_t)(start + c0 + col) * p.I + rb * 64 + q * 16 + half * 8) = w;
+  __syncwarp();  // the tile is rewritten by the next chunk
+}
+
 // FC2 chunk with the tile's pair ids and scaled routing weights staged in shared
 // memory by the same warp (st_pair / st_w, indexed by column): no global load on the
 // chunk's path.

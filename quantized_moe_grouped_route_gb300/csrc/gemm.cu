@@ -99,8 +99,8 @@ struct Cfg {
   static constexpr int kStageBytes = KS * kRawBytes;  // [KS codes blocks][KS scale blocks]
   static constexpr int kSlotCols = 64 * KS;
   static constexpr int kAccCol0 = SL * kSlotCols;  // TMEM: [A slots][acc: ACCB x NMW x NMAX]
-  // FC2 epilogue staging on the prefill schedule: per epilogue warp, a tile's pair ids
-  // and weights
+  // epilogue staging on the prefill schedule, per epilogue warp: a tile's pair ids and
+  // weights (FC2) or a 512-byte transpose tile (FC1)
   static constexpr int kEpiBytes = NMW == 1 ? 4 * NMAX * 8 : 0;
   static constexpr int kSmemBytes = SL * kBBytes + RS * kStageBytes + 1024 + kCtrlBytes + kEpiBytes;
   static constexpr int kThreads = gemm_threads(DG);
@@ -539,7 +539,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
               for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[m][g][c]);
             }
             if constexpr (FC1)
-              epilogue_chunk_fc1(p, v, lane, q, rb, start, rows, 16 * k, gsc);
+              epilogue_chunk_fc1_tr(p, v, lane, q, rb, start, rows, 16 * k, gsc,
+                                    reinterpret_cast<uint8_t*>(st_pair));
             else
               epilogue_chunk_fc2_staged(p, v, lane, q, rb, rows, 16 * k, st_pair, st_w);
           }
