@@ -265,7 +265,8 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
                                n_tiles, err, s);
   if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
-  e = launch_gather(x_dev, sorted_pair, offsets + E, top_k, H, P, xs, sms, s);
+  const bool pdl = forward_uses_pdl(rsched);
+  e = launch_gather(x_dev, sorted_pair, offsets + E, top_k, H, P, xs, sms, s, pdl);
   if (e != cudaSuccess || !mark(2)) return QMOE_ERR_CUDA;
 
   GemmParams p1;
@@ -300,7 +301,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   e = launch_gemm(GemmKind::kFc2, rsched, map_h, p2, sms, s);
   if (e != cudaSuccess || !mark(4)) return QMOE_ERR_CUDA;
 
-  e = launch_combine(ypart, topk_ids_dev, M, top_k, E, H, out_dev, sms, s);
+  e = launch_combine(ypart, topk_ids_dev, M, top_k, E, H, out_dev, sms, s, pdl);
   if (e != cudaSuccess || !mark(5)) return QMOE_ERR_CUDA;
   return QMOE_OK;
 }

@@ -561,7 +561,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 }
 
 template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1>
-cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream,
+               bool pdl = true) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW, KS>;
   auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, KS, BIN, FC1>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -573,11 +574,13 @@ cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaS
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, k, tmap, p);
 }
 
 }  // namespace
+
+bool forward_uses_pdl(int sched) { return sched != QMOE_SCHED_PREFILL; }
 
 int gemm_tile_n(int sched) {
   if (sched == QMOE_SCHED_DECODE) return 16;
@@ -612,8 +615,9 @@ cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, con
   if (sched == kSchedPrefillNarrow)
     return fc1 ? run<192, 8, 2, 2, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
                : run<192, 8, 2, 2, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
-  return fc1 ? run<320, 6, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
-             : run<320, 6, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
+  const bool pdl = forward_uses_pdl(sched);
+  return fc1 ? run<320, 6, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream, pdl)
+             : run<320, 6, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream, pdl);
 }
 
 }  // namespace qmoe

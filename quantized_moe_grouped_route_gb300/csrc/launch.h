@@ -17,10 +17,12 @@ cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* 
 // misc.cu
 cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
                           uint8_t* out_codes, uint8_t* out_scales, cudaStream_t stream);
+// pdl: launch with programmatic stream serialization (see pdl_attribute)
 cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
-                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream);
+                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream,
+                          bool pdl);
 cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
-                           void* out, int num_sms, cudaStream_t stream);
+                           void* out, int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_selftest_dequant(uint16_t* out, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(unsigned int* err, long long limit_ns, cudaStream_t stream);
 
@@ -46,6 +48,11 @@ struct GemmParams {
 
 // Launch attribute that lets a kernel start while the previous kernel on the stream
 // finishes (it must then call grid_dep_wait before reading that kernel's outputs).
+// The forward uses it on every schedule but the wide prefill one, where kernels that
+// take SMs early (and start their weight streams) slowed the layer by about 2%:
+// measured 4.63 against 4.54 ms on the large prefill workload, while decode (0.515
+// against 0.526 ms) and the narrow prefill schedule gain from the overlap.
+bool forward_uses_pdl(int sched);
 inline cudaLaunchAttribute pdl_attribute() {
   cudaLaunchAttribute a;
   a.id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -176,7 +176,8 @@ cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int 
 }
 
 cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
-                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream) {
+                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream,
+                          bool pdl) {
   const int chunks = H / 8;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
@@ -185,13 +186,13 @@ cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, gather_kernel, reinterpret_cast<const uint4*>(x), sorted_pair,
                             n_valid, top_k, chunks, reinterpret_cast<uint4*>(xs));
 }
 
 cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
-                           void* out, int num_sms, cudaStream_t stream) {
+                           void* out, int num_sms, cudaStream_t stream, bool pdl) {
   const long long work = (long long)M * (H / 8);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
@@ -199,7 +200,7 @@ cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int to
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, combine_kernel, ypart, ids, M, top_k, E, H,
                             reinterpret_cast<uint4*>(out));
 }
