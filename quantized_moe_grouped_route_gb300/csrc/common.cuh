@@ -164,16 +164,6 @@ __device__ __forceinline__ void tma_load_2d_if(uint32_t pred, uint32_t dst, cons
       : "memory");
 }
 
-// Prefetch of a 2-D tensor box into L2 by one lane (pred != 0), no shared memory
-// involved; x (innermost) must be a multiple of 8 bf16 elements.
-__device__ __forceinline__ void tma_prefetch_2d_if(uint32_t pred, const CUtensorMap* map, int x, int y) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
-      "@p cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%1, {%2, %3}];\n\t}" ::"r"(pred),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
-      : "memory");
-}
-
 // 3-D tiled tensor copy by one lane (pred != 0); x (innermost) must be a multiple of
 // 8 bf16 elements.
 __device__ __forceinline__ void tma_load_3d_if(uint32_t pred, uint32_t dst, const CUtensorMap* map,
