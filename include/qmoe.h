@@ -84,8 +84,9 @@ int qmoe_max_tiles(int M, int top_k, int E, int tile_n);
  *                    rows <= tile_n, experts ascending, positions ascending; only
  *                    the first *n_tiles entries are written.
  *   n_tiles_dev      int32 [1].
- *   workspace_dev    >= qmoe_route_workspace_size(...) bytes; its first 4 bytes are
- *                    the error word, which this call clears first.
+ *   workspace_dev    >= qmoe_route_workspace_size(...) bytes, 256-byte aligned; its
+ *                    first 4 bytes are the error word, which this call clears first;
+ *                    above 8192 pairs it also holds per-warp count tables.
  * The result is bit-exact and deterministic.
  */
 size_t qmoe_route_workspace_size(int M, int top_k, int E, int tile_n);

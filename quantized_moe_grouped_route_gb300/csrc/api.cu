@@ -77,7 +77,7 @@ int make_tmap_rows(CUtensorMap* map, const void* base, int rows, int cols, int b
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct ForwardLayout {
-  size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, xs, h, ypart, total;
+  size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, route_scratch, xs, h, ypart, total;
   int rows;  // rows of xs / h (>= 16, multiple of 16)
   int tile_n, max_tiles;
 };
@@ -117,7 +117,9 @@ ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {
   L.tiles = off;
   off = align_up(off + 12 * (size_t)L.max_tiles, 256);
   L.n_tiles = off;
-  off = align_up(off + 4, 1024);
+  off = align_up(off + 4, 256);
+  L.route_scratch = off;
+  off = align_up(off + route_scratch_bytes(P, E), 1024);
   L.xs = off;
   off = align_up(off + 2 * (size_t)L.rows * H, 1024);
   L.h = off;
@@ -157,11 +159,9 @@ int qmoe_max_tiles(int M, int top_k, int E, int tile_n) {
 }
 
 size_t qmoe_route_workspace_size(int M, int top_k, int E, int tile_n) {
-  (void)M;
-  (void)top_k;
-  (void)E;
   (void)tile_n;
-  return kWsHeaderBytes;
+  if (M < 0 || top_k < 1 || E < 1) return kWsHeaderBytes;
+  return kWsHeaderBytes + route_scratch_bytes((long long)M * top_k, E);
 }
 
 int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
@@ -173,6 +173,7 @@ int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
   if ((long long)M * top_k >= (1LL << 31) / 16) return QMOE_ERR_SHAPE;
   if (!offsets_dev || !n_tiles_dev || !workspace_dev || !tiles_dev) return QMOE_ERR_ARG;
   if (M > 0 && (!topk_ids_dev || !sorted_pair_dev || !pair_pos_dev)) return QMOE_ERR_ARG;
+  if ((uintptr_t)workspace_dev & 255) return QMOE_ERR_ARG;
   if (ws_bytes < qmoe_route_workspace_size(M, top_k, E, tile_n)) return QMOE_ERR_WORKSPACE;
   int sms = 0;
   int rc = device_info(&sms);
@@ -181,7 +182,8 @@ int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
   if (cudaMemsetAsync(workspace_dev, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
   return cuda_rc(launch_route(topk_ids_dev, M * top_k, E, tile_n, offsets_dev, sorted_pair_dev,
                               pair_pos_dev, tiles_dev, n_tiles_dev,
-                              reinterpret_cast<unsigned int*>(workspace_dev), s));
+                              reinterpret_cast<unsigned int*>(workspace_dev),
+                              reinterpret_cast<uint8_t*>(workspace_dev) + kWsHeaderBytes, s));
 }
 
 size_t qmoe_repacked_fp4_size(int E, int N, int K) {
@@ -263,7 +265,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   if (cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
   if (!mark(0)) return QMOE_ERR_CUDA;
   cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
-                               n_tiles, err, s);
+                               n_tiles, err, ws + L.route_scratch, s);
   if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
   const bool pdl = forward_uses_pdl(rsched);
   e = launch_gather(x_dev, sorted_pair, offsets + E, top_k, H, P, xs, sms, s, pdl);

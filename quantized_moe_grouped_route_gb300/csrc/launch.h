@@ -10,9 +10,11 @@ namespace qmoe {
 // route.cu
 constexpr int kRouteThreads = 512;
 size_t route_smem_bytes(int E);
+// scratch: route_scratch_bytes(P, E) bytes of device memory (none below 8193 pairs)
+size_t route_scratch_bytes(long long P, int E);
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
-                         unsigned int* err, cudaStream_t stream);
+                         unsigned int* err, void* scratch, cudaStream_t stream);
 
 // misc.cu
 cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,

@@ -6,8 +6,8 @@
 // discussion 2855.  The tile list cuts each expert's run of positions into tiles of
 // at most tile_n pairs, experts ascending.
 //
-// One block of 16 warps.  Each warp owns a contiguous range of pairs, so ranks come
-// out stable without any ordering between warps:
+// Warps of 32 lanes; each owns a contiguous range of pairs, the ranges in pair order,
+// so ranks come out stable without any ordering between warps:
 //   A. warp-aggregated histogram: lanes with equal expert ids find each other with
 //      match.any, the lowest such lane adds the group size to the warp's own row
 //      of a [16][E] count table (no atomics, no races);
@@ -15,6 +15,10 @@
 //      exclusive scan of tile counts, and each warp's starting position per expert;
 //   C. scatter: each warp walks its range again; a pair's position is its warp's
 //      running base for the expert plus its rank among equal lanes of the step.
+// Up to 8192 pairs this is one block of 16 warps with the count table in shared memory
+// (one launch: the decode case is launch-latency bound).  Larger inputs run A, B and C
+// as three kernels: A and C over up to 152 blocks (about 256 pairs per warp), with the
+// [blocks * 16][E] table in the workspace, B in one block.
 #include "common.cuh"
 #include "launch.h"
 
@@ -52,27 +56,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   return excl;
 }
 
-__global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const int32_t* __restrict__ ids, int P, int E, int T, int32_t* __restrict__ offsets,
-                 int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_pos,
-                 int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
-                 unsigned int* __restrict__ err) {
-  extern __shared__ int hist[];  // [kWarps][E]
-  __shared__ int scan_scratch[kWarps];
-  __shared__ int s_total;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = 0;
-  __syncthreads();
-
-  // contiguous range per warp, a whole number of 32-pair steps
-  const int chunk = (((P + kWarps - 1) / kWarps) + 31) & ~31;
-  const int lo = w * chunk;
-  const int hi = min(P, lo + chunk);
-  int* hw = hist + w * E;
+// A. warp-aggregated histogram of the pairs [lo, hi) into the warp's row hw[E]:
+// lanes with equal expert ids find each other with match.any and the lowest such lane
+// adds the group size.  The ids of kBatch steps are loaded before the first is used,
+// so a warp waits for global memory once per batch, not per step.  Returns whether an
+// id >= E was seen.
+__device__ __forceinline__ bool warp_histogram(const int32_t* __restrict__ ids, int lo, int hi, int E,
+                                               int* hw, int lane) {
   bool bad = false;
-
-  // A. warp-aggregated histogram.  The ids of kBatch steps are loaded before the
-  // first is used, so a warp waits for global memory once per batch, not per step.
   for (int base0 = lo; base0 < hi; base0 += 32 * kBatch) {
     int eb[kBatch];
 #pragma unroll
@@ -93,11 +84,16 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       __syncwarp();
     }
   }
-  if (bad) atomicOr(err, QMOE_FLAG_BAD_ID);
-  __syncthreads();
+  return bad;
+}
 
-  // B. totals, offsets, tile counts, per-warp bases.  Thread t owns experts
-  // [t*ept, (t+1)*ept).
+// B. From the R per-warp rows h[R][E] of counts (rows in pair order): offsets, the tile
+// list, and each row turned into that warp's first position per expert.  Thread t owns
+// experts [t*ept, (t+1)*ept).  Whole block; h in shared or global memory.
+__device__ __forceinline__ void route_scan(int* h, int R, int E, int T, int32_t* __restrict__ offsets,
+                                           int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
+                                           int* scan_scratch) {
+  const int tid = threadIdx.x;
   const int ept = (E + kRouteThreads - 1) / kRouteThreads;
   const int e0 = tid * ept;
   int my_pairs = 0, my_tiles = 0;
@@ -105,7 +101,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     const int e = e0 + j;
     if (e < E) {
       int c = 0;
-      for (int ww = 0; ww < kWarps; ++ww) c += hist[ww * E + e];
+      for (int r = 0; r < R; ++r) c += h[(size_t)r * E + e];
       my_pairs += c;
       my_tiles += (c + T - 1) / T;
     }
@@ -118,9 +114,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (e >= E) break;
     offsets[e] = pair_base;
     int run = pair_base;
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const int c = hist[ww * E + e];
-      hist[ww * E + e] = run;  // becomes warp ww's next position for expert e
+    for (int r = 0; r < R; ++r) {
+      const int c = h[(size_t)r * E + e];
+      h[(size_t)r * E + e] = run;  // becomes warp r's next position for expert e
       run += c;
     }
     const int cnt = run - pair_base;
@@ -135,11 +131,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   if (tid == 0) {
     offsets[E] = total_pairs;
     *n_tiles = total_tiles;
-    s_total = total_pairs;
   }
-  __syncthreads();
+}
 
-  // C. stable scatter (steps in order within each batch, batches in order)
+// C. stable scatter of the pairs [lo, hi) from the warp's running positions hw[E]
+// (steps in order within each batch, batches in order).
+__device__ __forceinline__ void warp_scatter(const int32_t* __restrict__ ids, int lo, int hi, int E,
+                                             int* hw, int lane, int32_t* __restrict__ sorted_pair,
+                                             int32_t* __restrict__ pair_pos) {
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int base0 = lo; base0 < hi; base0 += 32 * kBatch) {
     int eb[kBatch];
@@ -169,22 +168,122 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
       }
     }
   }
-  for (int pos = s_total + tid; pos < P; pos += kRouteThreads) sorted_pair[pos] = -1;
+}
+
+// Pairs per warp: contiguous ranges of whole 32-pair steps, in pair order over the
+// warps of all blocks (warp g = block * kWarps + warp), so ranks come out stable.
+__host__ __device__ __forceinline__ int route_chunk(int P, int nwarps) {
+  return (((P + nwarps - 1) / nwarps) + 31) & ~31;
+}
+
+// Small inputs: the whole route in one block of kWarps warps, rows in shared memory.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const int32_t* __restrict__ ids, int P, int E, int T, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_pos,
+                 int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
+                 unsigned int* __restrict__ err) {
+  extern __shared__ int hist[];  // [kWarps][E]
+  __shared__ int scan_scratch[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = 0;
+  __syncthreads();
+  const int chunk = route_chunk(P, kWarps);
+  const int lo = w * chunk;
+  const int hi = min(P, lo + chunk);
+  int* hw = hist + w * E;
+  if (warp_histogram(ids, lo, hi, E, hw, lane)) atomicOr(err, QMOE_FLAG_BAD_ID);
+  __syncthreads();
+  route_scan(hist, kWarps, E, T, offsets, tiles, n_tiles, scan_scratch);
+  __syncthreads();
+  warp_scatter(ids, lo, hi, E, hw, lane, sorted_pair, pair_pos);
+  for (int pos = offsets[E] + tid; pos < P; pos += kRouteThreads) sorted_pair[pos] = -1;
+}
+
+// Large inputs, three kernels over `blocks` blocks of kWarps warps; the per-warp rows
+// live in global memory (gh [blocks * kWarps][E]).
+__global__ void __launch_bounds__(kRouteThreads)
+    route_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int* __restrict__ gh,
+                      unsigned int* __restrict__ err) {
+  extern __shared__ int hist[];  // [kWarps][E]
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = 0;
+  __syncthreads();
+  const int chunk = route_chunk(P, gridDim.x * kWarps);
+  const int lo = min(P, (blockIdx.x * kWarps + w) * chunk);
+  const int hi = min(P, lo + chunk);
+  if (warp_histogram(ids, lo, hi, E, hist + w * E, lane)) atomicOr(err, QMOE_FLAG_BAD_ID);
+  __syncthreads();
+  int* dst = gh + (size_t)blockIdx.x * kWarps * E;
+  for (int i = tid; i < kWarps * E; i += kRouteThreads) dst[i] = hist[i];
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_scan_kernel(int R, int E, int T, int* __restrict__ gh, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+  __shared__ int scan_scratch[kWarps];
+  route_scan(gh, R, E, T, offsets, tiles, n_tiles, scan_scratch);
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+    route_scatter_kernel(const int32_t* __restrict__ ids, int P, int E, const int* __restrict__ gh,
+                         const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_pair,
+                         int32_t* __restrict__ pair_pos) {
+  extern __shared__ int hist[];  // [kWarps][E]: this block's warps' first positions
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int* src = gh + (size_t)blockIdx.x * kWarps * E;
+  for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = src[i];
+  __syncthreads();
+  const int chunk = route_chunk(P, gridDim.x * kWarps);
+  const int lo = min(P, (blockIdx.x * kWarps + w) * chunk);
+  const int hi = min(P, lo + chunk);
+  warp_scatter(ids, lo, hi, E, hist + w * E, lane, sorted_pair, pair_pos);
+  for (int pos = offsets[E] + blockIdx.x * kRouteThreads + tid; pos < P;
+       pos += gridDim.x * kRouteThreads)
+    sorted_pair[pos] = -1;
 }
 
 }  // namespace
 
 size_t route_smem_bytes(int E) { return (size_t)kWarps * (size_t)E * sizeof(int); }
 
+// Blocks of the multi-block route: about 256 pairs per warp (one batch of steps), at
+// most 152 blocks; inputs of up to 8192 pairs take the one-block kernel.
+int route_blocks(long long P) {
+  if (P <= 8192) return 1;
+  const long long b = (P + (long long)kWarps * 256 - 1) / ((long long)kWarps * 256);
+  return (int)(b < 152 ? b : 152);
+}
+
+size_t route_scratch_bytes(long long P, int E) {
+  const int b = route_blocks(P);
+  return b > 1 ? (size_t)b * kWarps * (size_t)E * sizeof(int) : 0;
+}
+
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
-                         unsigned int* err, cudaStream_t stream) {
+                         unsigned int* err, void* scratch, cudaStream_t stream) {
   const size_t smem = route_smem_bytes(E);
-  cudaError_t rc = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)smem);
+  const int blocks = route_blocks(P);
+  if (blocks == 1) {
+    cudaError_t rc = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
+    if (rc != cudaSuccess) return rc;
+    route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, P, E, tile_n, offsets, sorted_pair,
+                                                     pair_pos, tiles, n_tiles, err);
+    return cudaGetLastError();
+  }
+  int* gh = reinterpret_cast<int*>(scratch);
+  cudaError_t rc = cudaFuncSetAttribute(route_hist_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (rc == cudaSuccess)
+    rc = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
   if (rc != cudaSuccess) return rc;
-  route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, P, E, tile_n, offsets, sorted_pair, pair_pos,
-                                                   tiles, n_tiles, err);
+  route_hist_kernel<<<blocks, kRouteThreads, smem, stream>>>(ids, P, E, gh, err);
+  route_scan_kernel<<<1, kRouteThreads, 0, stream>>>(blocks * kWarps, E, tile_n, gh, offsets, tiles,
+                                                     n_tiles);
+  route_scatter_kernel<<<blocks, kRouteThreads, smem, stream>>>(ids, P, E, gh, offsets, sorted_pair,
+                                                                pair_pos);
   return cudaGetLastError();
 }
 

@@ -32,6 +32,9 @@ def test_size_queries(lib):
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_AUTO, 2048, 8, 128) == 192
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_PREFILL, 16, 8, 256) == 192
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_PREFILL_PAIR, 8192, 8, 256) == 256
+    # above 8192 pairs the route keeps per-warp count tables in its workspace
+    assert qmoe.qmoe_route_workspace_size(1024, 8, 256, 320) == 256
+    assert qmoe.qmoe_route_workspace_size(8192, 8, 256, 320) == 256 + 16 * 16 * 256 * 4
     assert qmoe.qmoe_repacked_fp4_size(256, 4096, 7168) == 256 * 4096 * 3584
     assert qmoe.qmoe_repacked_scale_size(256, 7168, 2048) == 256 * 7168 * 128
     ws = qmoe.qmoe_forward_workspace_size(8192, 7168, 2048, 256, 8)

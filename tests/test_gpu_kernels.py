@@ -101,7 +101,10 @@ def test_route_configs_bit_exact(cfg, tile_n):
 
 
 @pytest.mark.parametrize("case", ["neg_ids", "bad_ids", "one_expert", "all_same", "empty_experts",
-                                  "nothing_routed", "tile1", "big_E", "ragged"])
+                                  "nothing_routed", "tile1", "big_E", "ragged",
+                                  # above 8192 pairs: the three-kernel multi-block route
+                                  "mb_bad_ids", "mb_big_E", "mb_one_expert", "mb_just_above",
+                                  "mb_nothing_routed"])
 def test_route_edge_cases(case):
     rng = np.random.default_rng(zlib.crc32(case.encode()))
     if case == "neg_ids":
@@ -120,8 +123,18 @@ def test_route_edge_cases(case):
         ids, E, T = rng.integers(0, 5, size=(20, 3)), 5, 1
     elif case == "big_E":
         ids, E, T = rng.integers(0, 2048, size=(1000, 8)), 2048, 256
-    else:
+    elif case == "ragged":
         ids, E, T = rng.integers(0, 3, size=(1001, 1)), 3, 256
+    elif case == "mb_bad_ids":
+        ids, E, T = rng.integers(-2, 12, size=(3001, 3)), 10, 320
+    elif case == "mb_big_E":
+        ids, E, T = rng.integers(0, 2048, size=(2500, 8)), 2048, 192
+    elif case == "mb_one_expert":
+        ids, E, T = np.zeros((10000, 1)), 1, 320
+    elif case == "mb_just_above":
+        ids, E, T = rng.integers(0, 3, size=(8193, 1)), 3, 16
+    else:
+        ids, E, T = np.full((4097, 4), -1), 16, 320
     _check_route(torch.tensor(np.asarray(ids), dtype=torch.int32, device="cuda"), E, T)
 
 
