@@ -70,6 +70,9 @@ def _bind(lib):
     lib.qo_forward.restype = i32
     lib.qo_forward.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, i32, i32, P, i64, P, P,
                                i32]
+    lib.qo_forward_hl.restype = i32
+    lib.qo_forward_hl.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, i32, i32, P, i64, P, P,
+                                  i32, P, P, P, ctypes.c_double]
     lib.qo_forward_h.restype = i32
     lib.qo_forward_h.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, i32, i32, P, i64, P, P,
                                  i32, P, P, P]
@@ -135,7 +138,7 @@ def route(topk_ids, E: int, tile_n: int, lib=None):
 
 def forward(x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, tokens=None,
             nthreads: int | None = None, lib=None, return_f64: bool = False, check: bool = True,
-            h_given=None, return_h: bool = False):
+            h_given=None, return_h: bool = False, swiglu_limit: float | None = None):
     """The layer on the CPU in fp64 for `tokens` (default: all).  Returns bf16 bits as
     uint16 [n_tokens][H], plus (in this order, when asked) the fp64 values before the
     final rounding, and a dict with the h actually used ([n_tokens*top_k][I] bf16 bits)
@@ -143,7 +146,9 @@ def forward(x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, tokens=None,
 
     h_given ([n_tokens*top_k][I] bf16 bits, row t*top_k + k for the t-th listed token):
     bf16 roundings of h taken elsewhere (by the GPU); each is checked to be one of the
-    two bf16 values bracketing the exact SiLU(gate)*up and then used for FC2."""
+    two bf16 values bracketing the exact SiLU(gate)*up and then used for FC2.
+    swiglu_limit (> 0, None: no clamp): gate clamped to at most the limit and up to
+    [-limit, limit] before SiLU(gate)*up (the GLM form of the fc1 epilogue)."""
     lib = lib or _load()
     xb = _np(x, np.uint16)
     M, H = xb.shape
@@ -168,12 +173,13 @@ def forward(x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, tokens=None,
     hout = np.zeros((n * top_k, I), np.uint16) if return_h else None
     if nthreads is None:
         nthreads = lib.qo_max_threads()
-    rc = lib.qo_forward_h(_ptr(xb), _ptr(a13), _ptr(b13), _ptr(c13), _ptr(a2), _ptr(b2), _ptr(c2),
-                          _ptr(ids), _ptr(wts), M, H, I, E, top_k,
-                          _ptr(tok) if tok is not None else None, n, _ptr(out),
-                          _ptr(out64) if out64 is not None else None, nthreads,
-                          _ptr(hg) if hg is not None else None, _ptr(stats),
-                          _ptr(hout) if hout is not None else None)
+    limit = float("inf") if swiglu_limit is None else float(swiglu_limit)
+    rc = lib.qo_forward_hl(_ptr(xb), _ptr(a13), _ptr(b13), _ptr(c13), _ptr(a2), _ptr(b2), _ptr(c2),
+                           _ptr(ids), _ptr(wts), M, H, I, E, top_k,
+                           _ptr(tok) if tok is not None else None, n, _ptr(out),
+                           _ptr(out64) if out64 is not None else None, nthreads,
+                           _ptr(hg) if hg is not None else None, _ptr(stats),
+                           _ptr(hout) if hout is not None else None, limit)
     if check and rc < 0:
         raise ValueError(f"qo_forward failed: {rc}")
     res = [out]

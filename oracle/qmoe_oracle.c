@@ -11,7 +11,8 @@
  *    0..I-1 are up and I..2I-1 gate; w2 is [H][I/2]; global scale multiplies the
  *    accumulator), route_prep (a pair's slot is its rank among earlier pairs with
  *    the same expert; expert -1 is skipped), fc1_rm epilogue (SiLU(gate)*up, h
- *    rounded to a 16-bit type), fc2_rm epilogue (global scale times routing weight
+ *    rounded to a 16-bit type; the GLM clamp of gate from above and of up to
+ *    [-limit, limit] before the product), fc2_rm epilogue (global scale times routing weight
  *    times accumulator, written per (token, k) pair), combine (sum over k in k
  *    order, skipping pairs without an expert, rounded to bf16).
  *  - tilelang_kernels.py (grouped_gemm_fp4): per-expert dequantize-then-linear
@@ -28,6 +29,8 @@
  *  - h is rounded to bf16 (round to nearest, ties to even) after SiLU(gate)*up;
  *    every other intermediate stays fp64; the layer output is rounded to bf16.
  *  - SiLU(g) = g / (1 + exp(-g)).
+ *  - The SwiGLU limit L (qo_forward_hl; +infinity elsewhere, i.e. no clamp):
+ *    gate' = min(gate, L), up' = min(max(up, -L), L), h = bf16(SiLU(gate') * up').
  *  - Expert ids < 0 contribute nothing; ids >= E are invalid: they are skipped
  *    like -1 and the call returns QO_WARN_BAD_ID.
  *  - Routing weights are used as given (no renormalisation); a token may name the
@@ -225,12 +228,17 @@ static void bf16_bracket(double v, double* lo, double* hi) {
  * NULL, same layout as h_given) receives the h values used; rows of slots without an
  * expert are zero.
  */
-int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
-                 const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
-                 const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
-                 const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
-                 int nthreads, const uint16_t* h_given, int64_t* h_stats, uint16_t* h_out) {
+/* As qo_forward_h, with the SwiGLU limit swiglu_limit (> 0; +infinity: no clamp)
+ * applied to gate and up before h (fc1_rm epilogue, GLM variant).  The clamps are
+ * 1-Lipschitz, so the h_given check keeps its bound with the clamped gate and up. */
+int qo_forward_hl(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
+                  const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
+                  const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
+                  const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
+                  int nthreads, const uint16_t* h_given, int64_t* h_stats, uint16_t* h_out,
+                  double swiglu_limit) {
   if (M < 0 || H < 16 || I < 16 || H % 16 || I % 16 || E < 1 || top_k < 1) return QO_ERR_ARG;
+  if (!(swiglu_limit > 0.0)) return QO_ERR_ARG; /* also rejects NaN */
   if (tokens == NULL) n_tokens = M;
   for (int64_t t = 0; t < n_tokens; ++t) {
     int64_t m = tokens ? tokens[t] : t;
@@ -273,6 +281,9 @@ int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, cons
         }
         for (int64_t i = 0; i < I; ++i) {
           double up = g[i], gate = g[I + i];
+          if (gate > swiglu_limit) gate = swiglu_limit;
+          if (up > swiglu_limit) up = swiglu_limit;
+          if (up < -swiglu_limit) up = -swiglu_limit;
           double silu = gate / (1.0 + exp(-gate));
           double exact = silu * up;
           h[i] = qo_bf16_to_double(qo_bf16_rne(exact));
@@ -317,6 +328,15 @@ int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, cons
   }
   if (nan_scale) return QO_ERR_NAN_SCALE;
   return bad_id ? QO_WARN_BAD_ID : QO_OK;
+}
+
+int qo_forward_h(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
+                 const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
+                 const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
+                 const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
+                 int nthreads, const uint16_t* h_given, int64_t* h_stats, uint16_t* h_out) {
+  return qo_forward_hl(x, w13, s13, gs13, w2, s2, gs2, ids, topk_w, M, H, I, E, top_k, tokens,
+                       n_tokens, out_bf16, out_f64, nthreads, h_given, h_stats, h_out, INFINITY);
 }
 
 int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,

@@ -58,9 +58,10 @@ def dequant(w: np.ndarray, s: np.ndarray) -> np.ndarray:
     return vals * sc
 
 
-def forward(x_bf16_bits, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights):
+def forward(x_bf16_bits, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, swiglu_limit=None):
     """Returns the layer output [M][H] as float64 values of bf16 numbers, plus the
-    float64 sum before the final rounding."""
+    float64 sum before the final rounding.  swiglu_limit (None: none) clamps gate from
+    above and up to [-limit, limit] before SiLU(gate) * up."""
     x = (np.asarray(x_bf16_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
     x = x.astype(np.float64)
     M, H = x.shape
@@ -76,6 +77,9 @@ def forward(x_bf16_bits, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights):
         W2 = dequant(w2[e], s2[e]) * np.float64(gs2[e])       # [H][I]
         g = x[toks] @ W13.T                                   # [n][2I]
         up, gate = g[:, :I], g[:, I:]
+        if swiglu_limit is not None:
+            gate = np.minimum(gate, swiglu_limit)
+            up = np.clip(up, -swiglu_limit, swiglu_limit)
         h = round_bf16(gate / (1.0 + np.exp(-gate)) * up)
         y = h @ W2.T                                          # [n][H]
         contrib = y * topk_weights[toks, slots].astype(np.float64)[:, None]

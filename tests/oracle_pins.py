@@ -440,6 +440,79 @@ def pin_tiny_config(lib):
     assert np.array_equal(oracle.bf16_bits_to_float(out), twin_bf)
 
 
+def _permutation_layer(seed):
+    """up[i] = x[sig(i)], gate[i] = 2 x[tau(i)] exactly, out[j] = h[pi(j)]."""
+    rng = np.random.default_rng(seed)
+    M, H, I, E = 3, 48, 32, 2
+    t = _zeros(M, H, I, E, 2)
+    t["x"] = _rand_bf16(rng, (M, H))
+    sig = rng.permutation(H)[:I]
+    tau = rng.permutation(H)[:I]
+    pi = rng.integers(0, I, size=H)
+    e = 1
+    for i in range(I):
+        _set_code(t["w13"], t["s13"], e, i, int(sig[i]), 0x2, 0x40)       # 1.0 * 2.0
+        _set_code(t["w13"], t["s13"], e, I + i, int(tau[i]), 0x4, 0x40)   # 2.0 * 2.0
+    for j in range(H):
+        _set_code(t["w2"], t["s2"], e, j, int(pi[j]), 0xA, 0x30)           # -1.0 * 0.5
+    t["gs13"][e] = 0.5
+    t["gs2"][e] = -2.0
+    t["topk_ids"][:] = [[e, -1], [-1, e], [e, 0]]
+    t["topk_weights"][:] = [[1.0, 9.0], [3.0, 1.0], [1.0, 0.0]]
+    return t, sig, tau, pi
+
+
+def pin_swiglu_limit(lib):
+    """GLM SwiGLU clamp on permutation-matrix weights: with gate = 2 x[tau(i)] and
+    up = x[sig(i)] exact, h = bf16(silu(min(gate, L)) * min(max(up, -L), L)) in closed
+    form, for limits that clamp many gates and ups from either side."""
+    n_gate = n_up_hi = n_up_lo = 0
+    for seed, L in ((31, 0.75), (32, 0.3), (33, 2.5)):
+        t, sig, tau, pi = _permutation_layer(seed)
+        out = _run(lib, t, swiglu_limit=L)
+        for m in range(t["x"].shape[0]):
+            xm = [bits_to_f(int(b)) for b in t["x"][m]]
+            h = []
+            for i in range(len(sig)):
+                g, u = 2.0 * xm[tau[i]], xm[sig[i]]
+                n_gate += g > L
+                n_up_hi += u > L
+                n_up_lo += u < -L
+                h.append(bits_to_f(brute_bf16(silu(min(g, L)) * min(max(u, -L), L))))
+            for j in range(t["x"].shape[1]):
+                assert int(out[m, j]) == brute_bf16(h[pi[j]]), (seed, m, j)
+    assert n_gate and n_up_hi and n_up_lo  # each clamp was exercised
+
+
+def pin_swiglu_limit_infinite(lib):
+    """A limit above every |gate| and |up| (or +infinity) changes nothing; a limit of 0
+    or below is rejected."""
+    t = _random_layer(34)
+    ref, ref64 = _run(lib, t, return_f64=True)
+    for L in (float("inf"), 1e30):
+        out, f64 = _run(lib, t, return_f64=True, swiglu_limit=L)
+        assert np.array_equal(out, ref) and np.array_equal(f64, ref64)
+    for L in (0.0, -1.0, float("nan")):
+        try:
+            _run(lib, t, swiglu_limit=L)
+        except ValueError:
+            continue
+        raise AssertionError(f"limit {L} accepted")
+
+
+def pin_swiglu_limit_numpy_twin(lib):
+    from oracle import ref_numpy
+    t = _random_layer(35, M=5, H=64, I=48, E=3, top_k=2)
+    for L in (0.5, 1.5):
+        out, f64 = _run(lib, t, return_f64=True, swiglu_limit=L)
+        twin_bf, twin64 = ref_numpy.forward(t["x"], t["w13"], t["s13"], t["gs13"], t["w2"],
+                                            t["s2"], t["gs2"], t["topk_ids"], t["topk_weights"],
+                                            swiglu_limit=L)
+        assert np.allclose(f64, twin64, rtol=1e-11, atol=1e-14)
+        assert np.array_equal(oracle.bf16_bits_to_float(out), twin_bf)
+
+
 ALL_PINS = [pin_e2m1, pin_e4m3, pin_bf16_decode, pin_bf16_round, pin_route, pin_zero_weights,
             pin_single_nibble, pin_h_given, pin_permutation_blocks, pin_subnormal_scale, pin_token_permutation,
-            pin_duplicate_expert, pin_weight_linearity, pin_numpy_twin, pin_tiny_config]
+            pin_duplicate_expert, pin_weight_linearity, pin_numpy_twin, pin_tiny_config,
+            pin_swiglu_limit, pin_swiglu_limit_infinite, pin_swiglu_limit_numpy_twin]

@@ -49,6 +49,12 @@ MUTANTS = {
                        "    int64_t pos = offsets[e + 1] - 1 - seen[e];\n    seen[e] += 1;"),
     "tile_rows": ("if (rows > tile_n) rows = tile_n;", "if (rows >= tile_n) rows = tile_n - 1;"),
     "bad_id_counted": ("if (e >= 0 && e < E) count[e] += 1;", "if (e >= 0 && e < E) count[e] += 1; else if (e >= E) count[E-1] += 1;"),
+    "limit_gate_ignored": ("if (gate > swiglu_limit) gate = swiglu_limit;", ";"),
+    "limit_gate_two_sided": ("if (gate > swiglu_limit) gate = swiglu_limit;",
+                             "if (gate > swiglu_limit) gate = swiglu_limit; if (gate < -swiglu_limit) gate = -swiglu_limit;"),
+    "limit_up_one_sided": ("if (up < -swiglu_limit) up = -swiglu_limit;", ";"),
+    "limit_after_silu": ("double silu = gate / (1.0 + exp(-gate));",
+                         "double silu = g[I + i] / (1.0 + exp(-g[I + i]));"),
     "skip_negative_slot_wrong": ("        if (e < 0) continue;\n        if (e >= E) {", "        if (e < 0) e = 0;\n        if (e >= E) {"),
 }
 
