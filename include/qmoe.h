@@ -141,6 +141,23 @@ int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8
                       size_t ws_bytes, void* stream);
 
 /*
+ * moe_nvfp4_forward_limit — moe_nvfp4_forward with the GLM form of the SwiGLU
+ * (megamoe_rm.cu page, fc1_rm epilogue): before h = bf16(SiLU(gate) * up), gate is
+ * clamped from above and up to [-swiglu_limit, swiglu_limit].
+ *   swiglu_limit  > 0; +infinity gives exactly moe_nvfp4_forward's results; zero,
+ *                 negative or NaN: QMOE_ERR_ARG.
+ * Other arguments, results and errors as moe_nvfp4_forward.  With a finite limit
+ * QMOE_SCHED_PREFILL_PAIR runs as QMOE_SCHED_PREFILL.
+ */
+int moe_nvfp4_forward_limit(const void* x_dev, const uint8_t* w13_fp4_dev,
+                            const uint8_t* w13_scale_dev, const float* w13_gscale_dev,
+                            const uint8_t* w2_fp4_dev, const uint8_t* w2_scale_dev,
+                            const float* w2_gscale_dev, const int32_t* topk_ids_dev,
+                            const float* topk_weights_dev, void* out_dev, int M, int H, int I,
+                            int E, int top_k, int sched, float swiglu_limit, void* workspace_dev,
+                            size_t ws_bytes, void* stream);
+
+/*
  * moe_nvfp4_forward_noalloc — moe_nvfp4_forward for callers that cannot allocate
  * device memory: a plugin called from inside another runtime's enqueue step with no
  * allocator handed to it, a C host program that does not own the process's memory

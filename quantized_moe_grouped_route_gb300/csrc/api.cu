@@ -2,6 +2,7 @@
 // the launch sequence of the layer (megamoe_rm.cu page, megamoe_rm_forward: shape
 // checks, scratch carved from caller memory, everything on the caller's stream).
 #include <cudaTypedefs.h>
+#include <math.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -222,10 +223,12 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
                         const uint8_t* w2_scale_dev, const float* w2_gscale_dev,
                         const int32_t* topk_ids_dev, const float* topk_weights_dev, void* out_dev,
                         int M, int H, int I, int E, int top_k, int sched, void* workspace_dev,
-                        size_t ws_bytes, void* stream, void* const* events) {
+                        size_t ws_bytes, void* stream, void* const* events,
+                        float swiglu_limit = INFINITY) {
   int rc = check_shape(M, H, I, E, top_k);
   if (rc != QMOE_OK) return rc;
   if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
+  if (!(swiglu_limit > 0.0f)) return QMOE_ERR_ARG;  // also NaN
   if (M == 0) return QMOE_OK;
   if (!x_dev || !w13_fp4_dev || !w13_scale_dev || !w13_gscale_dev || !w2_fp4_dev ||
       !w2_scale_dev || !w2_gscale_dev || !topk_ids_dev || !topk_weights_dev || !out_dev ||
@@ -282,6 +285,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p1.nrb = 2 * I / 128;
   p1.h = h;
   p1.I = I;
+  p1.swiglu_limit = swiglu_limit;
   p1.err = err;
   e = launch_gemm(GemmKind::kFc1, rsched, map_x, p1, sms, s);
   if (e != cudaSuccess || !mark(3)) return QMOE_ERR_CUDA;
@@ -330,6 +334,18 @@ int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8
   return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
                       w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
                       sched, workspace_dev, ws_bytes, stream, nullptr);
+}
+
+int moe_nvfp4_forward_limit(const void* x_dev, const uint8_t* w13_fp4_dev,
+                            const uint8_t* w13_scale_dev, const float* w13_gscale_dev,
+                            const uint8_t* w2_fp4_dev, const uint8_t* w2_scale_dev,
+                            const float* w2_gscale_dev, const int32_t* topk_ids_dev,
+                            const float* topk_weights_dev, void* out_dev, int M, int H, int I,
+                            int E, int top_k, int sched, float swiglu_limit, void* workspace_dev,
+                            size_t ws_bytes, void* stream) {
+  return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
+                      w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
+                      sched, workspace_dev, ws_bytes, stream, nullptr, swiglu_limit);
 }
 
 int moe_nvfp4_forward_noalloc(const void* x_dev, const uint8_t* w13_fp4_dev,

@@ -26,6 +26,17 @@ __device__ __forceinline__ float silu_mul(float gate, float up) {
   return __fdividef(gate, 1.0f + e) * up;
 }
 
+// The GLM form of the SwiGLU (megamoe_rm.cu page, fc1_rm epilogue): gate clamped from
+// above and up to [-limit, limit] before SiLU(gate) * up.  CLAMP false leaves both.
+template <bool CLAMP>
+__device__ __forceinline__ void swiglu_clamp(float& gate, float& up, float limit) {
+  if constexpr (CLAMP) {
+    gate = fminf(gate, limit);
+    up = fminf(fmaxf(up, -limit), limit);
+  }
+}
+
+template <bool CLAMP = false>
 __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const float (&v)[16],
                                                    int lane, int q, int rb, int start, int rows,
                                                    int c0, float gsc) {
@@ -43,8 +54,9 @@ __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const fl
   for (int c = 0; c < 16; c += 2) {
     const float send = (is_up ? v[c + 1] : v[c]) * gsc;
     const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-    const float up = is_up ? v[c] * gsc : recv;
-    const float gate = is_up ? recv : v[c + 1] * gsc;
+    float up = is_up ? v[c] * gsc : recv;
+    float gate = is_up ? recv : v[c + 1] * gsc;
+    swiglu_clamp<CLAMP>(gate, up, p.swiglu_limit);
     hv[c >> 1] = silu_mul(gate, up);
   }
 #pragma unroll
@@ -59,6 +71,7 @@ __device__ __forceinline__ void epilogue_chunk_fc1(const GemmParams& p, const fl
 // fill rows 32 bytes apart, no bank conflicts) and come out as 16-byte rows, so each
 // lane writes one 16-byte piece of a pair's h row: one global store per lane and
 // chunk instead of eight 2-byte ones (global store issue dominates this epilogue).
+template <bool CLAMP = false>
 __device__ __forceinline__ void epilogue_chunk_fc1_tr(const GemmParams& p, const float (&v)[16],
                                                       int lane, int q, int rb, int start, int rows,
                                                       int c0, float gsc, uint8_t* tile) {
@@ -68,8 +81,9 @@ __device__ __forceinline__ void epilogue_chunk_fc1_tr(const GemmParams& p, const
   for (int c = 0; c < 16; c += 2) {
     const float send = (is_up ? v[c + 1] : v[c]) * gsc;
     const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-    const float up = is_up ? v[c] * gsc : recv;
-    const float gate = is_up ? recv : v[c + 1] * gsc;
+    float up = is_up ? v[c] * gsc : recv;
+    float gate = is_up ? recv : v[c + 1] * gsc;
+    swiglu_clamp<CLAMP>(gate, up, p.swiglu_limit);
     hv[c >> 1] = silu_mul(gate, up);
   }
   __nv_bfloat16* const t = reinterpret_cast<__nv_bfloat16*>(tile) + (lane & 15);
@@ -123,7 +137,7 @@ __device__ __forceinline__ void epilogue_stage_fc2(const GemmParams& p, int lane
 // forms the SiLU with expf and an IEEE division (FC1).  The decode schedule uses it for
 // both GEMMs (there the epilogue overlaps the next unit's MMAs, and this form kept the
 // dequant loop fastest), the prefill schedules for FC2.
-template <bool FC1>
+template <bool FC1, bool CLAMP = false>
 __device__ __forceinline__ void epilogue_chunk_small(const GemmParams& p, const float (&v)[16],
                                                      int lane, int q, int rb, int start, int rows,
                                                      int c0, float gsc) {
@@ -139,8 +153,9 @@ __device__ __forceinline__ void epilogue_chunk_small(const GemmParams& p, const 
     for (int c = 0; c < 16; c += 2) {
       const float send = (is_up ? v[c + 1] : v[c]) * gsc;
       const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-      const float up = is_up ? v[c] * gsc : recv;
-      const float gate = is_up ? recv : v[c + 1] * gsc;
+      float up = is_up ? v[c] * gsc : recv;
+      float gate = is_up ? recv : v[c + 1] * gsc;
+      swiglu_clamp<CLAMP>(gate, up, p.swiglu_limit);
       const int col = c0 + c + (is_up ? 0 : 1);
       if (col < rows) {
         const float hv = gate / (1.0f + expf(-gate)) * up;

@@ -28,6 +28,8 @@
 // Every wait is bounded (qmoe::mbar_wait): on expiry the CTA raises the timeout bit
 // in the error word, the roles leave their loops, in-flight copies and MMAs are
 // drained with bounded waits, and TMEM is released before the CTA exits.
+#include <cmath>
+
 #include "common.cuh"
 #include "dequant.cuh"
 #include "epilogue.cuh"
@@ -125,7 +127,8 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1,
+          bool CLAMP = false>
 __global__ void __launch_bounds__(gemm_threads(DG), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW, KS>;
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
           }
-          epilogue_chunk_small<FC1>(p, v, lane, q, rb, start, rows, c0, gsc);
+          epilogue_chunk_small<FC1, CLAMP>(p, v, lane, q, rb, start, rows, c0, gsc);
         }
       } else {
         // warp m holds MMAs of this unit iff its first step ks0 = (m - it0 % NMW) mod NMW
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
               for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[m][g][c]);
             }
             if constexpr (FC1)
-              epilogue_chunk_fc1_tr(p, v, lane, q, rb, start, rows, 16 * k, gsc,
+              epilogue_chunk_fc1_tr<CLAMP>(p, v, lane, q, rb, start, rows, 16 * k, gsc,
                                     reinterpret_cast<uint8_t*>(st_pair));
             else
               epilogue_chunk_fc2_staged(p, v, lane, q, rb, rows, 16 * k, st_pair, st_w);
@@ -560,11 +563,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   }
 }
 
-template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1>
+template <int NMAX, int RS, int SL, int ACCB, int DG, int NMW, int KS, bool BIN, bool FC1,
+          bool CLAMP = false>
 cudaError_t run(const CUtensorMap& tmap, const GemmParams& p, int num_sms, cudaStream_t stream,
                bool pdl = true) {
   using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW, KS>;
-  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, KS, BIN, FC1>;
+  auto* k = moe_gemm_kernel<NMAX, RS, SL, ACCB, DG, NMW, KS, BIN, FC1, CLAMP>;
   cudaError_t rc = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (rc != cudaSuccess) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -607,15 +611,23 @@ int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream) {
   const bool fc1 = kind == GemmKind::kFc1;
-  if (sched == QMOE_SCHED_DECODE)
+  // FC1 with a finite SwiGLU limit runs the clamping instantiations (the two-SM
+  // schedule then runs as the one-SM prefill one)
+  const bool clamp = fc1 && std::isfinite(p.swiglu_limit);
+  if (sched == QMOE_SCHED_DECODE) {
+    if (clamp) return run<16, 9, 3, 2, 3, 3, 2, true, true, true>(tmap_b, p, num_sms, stream);
     return fc1 ? run<16, 9, 3, 2, 3, 3, 2, true, true>(tmap_b, p, num_sms, stream)
                : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, num_sms, stream);
-  if (sched == QMOE_SCHED_PREFILL_PAIR && p.nrb % 2 == 0 && num_sms >= 2)
+  }
+  if (sched == QMOE_SCHED_PREFILL_PAIR && !clamp && p.nrb % 2 == 0 && num_sms >= 2)
     return launch_gemm2(kind, tmap_b, p, num_sms, stream);
-  if (sched == kSchedPrefillNarrow)
+  if (sched == kSchedPrefillNarrow) {
+    if (clamp) return run<192, 8, 2, 2, 2, 1, 1, false, true, true>(tmap_b, p, num_sms, stream);
     return fc1 ? run<192, 8, 2, 2, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream)
                : run<192, 8, 2, 2, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream);
+  }
   const bool pdl = forward_uses_pdl(sched);
+  if (clamp) return run<320, 6, 2, 1, 2, 1, 1, false, true, true>(tmap_b, p, num_sms, stream, pdl);
   return fc1 ? run<320, 6, 2, 1, 2, 1, 1, false, true>(tmap_b, p, num_sms, stream, pdl)
              : run<320, 6, 2, 1, 2, 1, 1, false, false>(tmap_b, p, num_sms, stream, pdl);
 }

@@ -37,9 +37,10 @@ struct GemmParams {
   const int32_t* n_tiles;     // [1]
   int K;                      // contraction length
   int nrb;                    // 128-row weight blocks per expert
-  // FC1 output: h [rows][I] bf16
+  // FC1 output: h [rows][I] bf16; the SwiGLU limit (+infinity: none)
   void* h;
   int I;
+  float swiglu_limit;
   // FC2 output: ypart [pairs][H] fp32
   float* ypart;
   const int32_t* sorted_pair;

@@ -73,6 +73,8 @@ def _bind(L):
         "qmoe_forward_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "moe_nvfp4_forward": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
                                     sz, P]),
+        "moe_nvfp4_forward_limit": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                          i32, ctypes.c_float, P, sz, P]),
         "moe_nvfp4_forward_noalloc": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                             i32, P]),
         "moe_nvfp4_forward_events": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
@@ -217,8 +219,9 @@ def moe_nvfp4_repack(w_fp4: torch.Tensor, w_scale: torch.Tensor, which: int, str
 def moe_nvfp4_forward(x, w13_fp4, w13_scale, w13_gscale, w2_fp4, w2_scale, w2_gscale, topk_ids,
                       topk_weights, out=None, *, H: int, I: int, E: int,
                       sched: int = QMOE_SCHED_AUTO, workspace: Optional[torch.Tensor] = None,
-                      stream=None) -> torch.Tensor:
-    """The layer.  w13_* / w2_* are the repacked weights from moe_nvfp4_repack."""
+                      stream=None, swiglu_limit: Optional[float] = None) -> torch.Tensor:
+    """The layer.  w13_* / w2_* are the repacked weights from moe_nvfp4_repack.
+    swiglu_limit (> 0): the GLM SwiGLU clamp (moe_nvfp4_forward_limit); None: none."""
     _need(x, torch.bfloat16, "x")
     _need(topk_ids, torch.int32, "topk_ids")
     _need(topk_weights, torch.float32, "topk_weights")
@@ -234,11 +237,21 @@ def moe_nvfp4_forward(x, w13_fp4, w13_scale, w13_gscale, w2_fp4, w2_scale, w2_gs
     wsb = qmoe_forward_workspace_size(M, H, I, E, top_k, sched)
     if workspace is None:
         workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=x.device)
-    rc = lib().moe_nvfp4_forward(_ptr(x), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w13_gscale),
-                                 _ptr(w2_fp4), _ptr(w2_scale), _ptr(w2_gscale), _ptr(topk_ids),
-                                 _ptr(topk_weights), _ptr(out), M, H, I, E, top_k, sched,
-                                 _ptr(workspace), workspace.numel(), _stream(stream))
-    _check("moe_nvfp4_forward", rc)
+    if swiglu_limit is None:
+        rc = lib().moe_nvfp4_forward(_ptr(x), _ptr(w13_fp4), _ptr(w13_scale), _ptr(w13_gscale),
+                                     _ptr(w2_fp4), _ptr(w2_scale), _ptr(w2_gscale),
+                                     _ptr(topk_ids), _ptr(topk_weights), _ptr(out), M, H, I, E,
+                                     top_k, sched, _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+        _check("moe_nvfp4_forward", rc)
+    else:
+        rc = lib().moe_nvfp4_forward_limit(_ptr(x), _ptr(w13_fp4), _ptr(w13_scale),
+                                           _ptr(w13_gscale), _ptr(w2_fp4), _ptr(w2_scale),
+                                           _ptr(w2_gscale), _ptr(topk_ids), _ptr(topk_weights),
+                                           _ptr(out), M, H, I, E, top_k, sched,
+                                           float(swiglu_limit), _ptr(workspace),
+                                           workspace.numel(), _stream(stream))
+        _check("moe_nvfp4_forward_limit", rc)
     return out
 
 
@@ -315,8 +328,10 @@ class NVFP4MoE:
                                    device=device or self.w13c.device)
         return self._ws
 
-    def __call__(self, x, topk_ids, topk_weights, out=None, sched=QMOE_SCHED_AUTO, stream=None):
+    def __call__(self, x, topk_ids, topk_weights, out=None, sched=QMOE_SCHED_AUTO, stream=None,
+                 swiglu_limit=None):
         ws = self.workspace(x.shape[0], topk_ids.shape[1], sched, x.device)
         return moe_nvfp4_forward(x, self.w13c, self.w13s, self.gs13, self.w2c, self.w2s, self.gs2,
                                  topk_ids, topk_weights, out, H=self.H, I=self.I, E=self.E,
-                                 sched=sched, workspace=ws, stream=stream)
+                                 sched=sched, workspace=ws, stream=stream,
+                                 swiglu_limit=swiglu_limit)

@@ -38,13 +38,14 @@ def check_close(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = ""):
 MAX_FLIP_RATE = 5e-3
 
 
-def oracle_forward(li, tokens=None, nthreads=None, h_given=None):
+def oracle_forward(li, tokens=None, nthreads=None, h_given=None, swiglu_limit=None):
     """Oracle output (bf16 bits) for the sampled tokens of a LayerInputs (any device);
     with h_given, also the h-decision statistics."""
     cpu = lambda t: t.detach().cpu()  # noqa: E731
     return oracle.forward(cpu(li.x), cpu(li.w13), cpu(li.s13), cpu(li.gs13), cpu(li.w2),
                           cpu(li.s2), cpu(li.gs2), cpu(li.topk_ids), cpu(li.topk_weights),
-                          tokens=tokens, nthreads=nthreads, h_given=h_given)
+                          tokens=tokens, nthreads=nthreads, h_given=h_given,
+                          swiglu_limit=swiglu_limit)
 
 
 def gpu_h_rows(ws, li, sched, tokens) -> np.ndarray:
@@ -64,7 +65,7 @@ def gpu_h_rows(ws, li, sched, tokens) -> np.ndarray:
     return out
 
 
-def check_layer(li, out, ws, sched, tokens=None, what=""):
+def check_layer(li, out, ws, sched, tokens=None, what="", swiglu_limit=None):
     """Parity of one forward call: (1) every GPU h value is one of the two bf16 values
     bracketing the exact SiLU(gate)*up and at most MAX_FLIP_RATE of them differ from
     the oracle's own rounding; (2) the outputs match the oracle fed those h decisions,
@@ -72,7 +73,7 @@ def check_layer(li, out, ws, sched, tokens=None, what=""):
     M = li.x.shape[0]
     toks = np.arange(M) if tokens is None else np.asarray(tokens)
     hg = gpu_h_rows(ws, li, sched, toks)
-    ref, st = oracle_forward(li, tokens=toks, h_given=hg)
+    ref, st = oracle_forward(li, tokens=toks, h_given=hg, swiglu_limit=swiglu_limit)
     assert st["outside"] == 0, f"{what}: {st['outside']} h values outside their bf16 bracket"
     assert st["flipped"] <= MAX_FLIP_RATE * max(st["compared"], 1), \
         f"{what}: {st['flipped']} of {st['compared']} h roundings differ"
@@ -81,10 +82,10 @@ def check_layer(li, out, ws, sched, tokens=None, what=""):
     return {"h_compared": st["compared"], "h_flipped": st["flipped"], "max_ratio": ratio}
 
 
-def gpu_forward(li, sched, layer=None):
+def gpu_forward(li, sched, layer=None, swiglu_limit=None):
     from quantized_moe_grouped_route_gb300 import NVFP4MoE
     if layer is None:
         layer = NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
-    out = layer(li.x, li.topk_ids, li.topk_weights, sched=sched)
+    out = layer(li.x, li.topk_ids, li.topk_weights, sched=sched, swiglu_limit=swiglu_limit)
     torch.cuda.synchronize()
     return out, layer

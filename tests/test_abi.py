@@ -66,6 +66,17 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
     rc = lib.moe_nvfp4_forward(null, null, null, null, null, null, null, null, null, null,
                                0, 128, 128, 8, 2, 0, null, 0, null)
     assert rc == qmoe.QMOE_OK
+    # SwiGLU limit: zero, negative or NaN rejected before anything else is looked at
+    # (zero tokens included); +infinity and positive limits pass to the pointer checks
+    for bad in (0.0, -1.0, float("nan")):
+        for M in (4, 0):
+            rc = lib.moe_nvfp4_forward_limit(null, null, null, null, null, null, null, null, null,
+                                             null, M, 128, 128, 8, 2, 0, bad, null, 0, null)
+            assert rc == qmoe.QMOE_ERR_ARG, (bad, M)
+    for good in (float("inf"), 7.0):
+        rc = lib.moe_nvfp4_forward_limit(null, null, null, null, null, null, null, null, null,
+                                         null, 0, 128, 128, 8, 2, 0, good, null, 0, null)
+        assert rc == qmoe.QMOE_OK
     # repack: bad role, bad shape
     assert lib.moe_nvfp4_repack(null, null, 1, 128, 128, 3, null, null, null) == qmoe.QMOE_ERR_ARG
     assert lib.moe_nvfp4_repack(null, null, 1, 100, 128, 1, null, null, null) == qmoe.QMOE_ERR_SHAPE
