@@ -107,6 +107,23 @@ int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
  *   out_scale_dev uint8, qmoe_repacked_scale_size(E, N, K) bytes
  * N % 128 == 0 and K % 128 == 0 are required (QMOE_ERR_SHAPE otherwise).
  */
+/*
+ * moe_nvfp4_repack_layout — moe_nvfp4_repack taking the block scales in one of two
+ * layouts (output identical for the same scale values):
+ *   QMOE_SCALES_PLAIN          [E][N][K/16], row-major (as moe_nvfp4_repack)
+ *   QMOE_SCALES_SWIZZLED_128X4 per expert N*K/16 bytes in the 128x4 swizzle that
+ *       CUTLASS / FlashInfer NVFP4 checkpoints keep (megamoe_rm.cu page, scale_off):
+ *       tiles of 128 rows x 4 scales, 512 bytes each, the 4-column tile index
+ *       fastest; inside a tile the scale of row r, column c at
+ *       (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.
+ * Other arguments and errors as moe_nvfp4_repack; an unknown layout: QMOE_ERR_ARG.
+ */
+#define QMOE_SCALES_PLAIN 0
+#define QMOE_SCALES_SWIZZLED_128X4 1
+int moe_nvfp4_repack_layout(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N,
+                            int K, int which, int scale_layout, uint8_t* out_fp4_dev,
+                            uint8_t* out_scale_dev, void* stream);
+
 size_t qmoe_repacked_fp4_size(int E, int N, int K);
 size_t qmoe_repacked_scale_size(int E, int N, int K);
 int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N, int K,

@@ -9,4 +9,4 @@ from .qmoe import (  # noqa: F401
     qmoe_max_tiles, qmoe_read_error, qmoe_repacked_fp4_size, qmoe_repacked_scale_size,
     qmoe_route_workspace_size, qmoe_sched_tile_n, qmoe_selftest_dequant, qmoe_selftest_timeout,
     QMOE_SCHED_AUTO, QMOE_SCHED_DECODE, QMOE_SCHED_PREFILL, QMOE_SCHED_PREFILL_PAIR, QMOE_W13,
-    QMOE_W2)
+    QMOE_W2, QMOE_SCALES_PLAIN, QMOE_SCALES_SWIZZLED_128X4)

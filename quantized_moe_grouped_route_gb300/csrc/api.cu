@@ -197,9 +197,12 @@ size_t qmoe_repacked_scale_size(int E, int N, int K) {
   return (size_t)E * N * (K / 16);
 }
 
-int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N, int K,
-                     int which, uint8_t* out_fp4_dev, uint8_t* out_scale_dev, void* stream) {
+int moe_nvfp4_repack_layout(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N,
+                            int K, int which, int scale_layout, uint8_t* out_fp4_dev,
+                            uint8_t* out_scale_dev, void* stream) {
   if (which != QMOE_W13 && which != QMOE_W2) return QMOE_ERR_ARG;
+  if (scale_layout != QMOE_SCALES_PLAIN && scale_layout != QMOE_SCALES_SWIZZLED_128X4)
+    return QMOE_ERR_ARG;
   if (E < 1 || E > 2048 || N < 128 || K < 128 || N % 128 || K % 128 || N > 131072 || K > 65536)
     return QMOE_ERR_SHAPE;
   if (!w_fp4_dev || !w_scale_dev || !out_fp4_dev || !out_scale_dev) return QMOE_ERR_ARG;
@@ -209,8 +212,15 @@ int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E
   int sms = 0;
   int rc = device_info(&sms);
   if (rc != QMOE_OK) return rc;
-  return cuda_rc(launch_repack(w_fp4_dev, w_scale_dev, E, N, K, which == QMOE_W13, out_fp4_dev,
+  return cuda_rc(launch_repack(w_fp4_dev, w_scale_dev, E, N, K, which == QMOE_W13,
+                               scale_layout == QMOE_SCALES_SWIZZLED_128X4, out_fp4_dev,
                                out_scale_dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N, int K,
+                     int which, uint8_t* out_fp4_dev, uint8_t* out_scale_dev, void* stream) {
+  return moe_nvfp4_repack_layout(w_fp4_dev, w_scale_dev, E, N, K, which, QMOE_SCALES_PLAIN,
+                                 out_fp4_dev, out_scale_dev, stream);
 }
 
 size_t qmoe_forward_workspace_size(int M, int H, int I, int E, int top_k, int sched) {

@@ -18,7 +18,8 @@ cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* 
 
 // misc.cu
 cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
-                          uint8_t* out_codes, uint8_t* out_scales, cudaStream_t stream);
+                          bool swizzled_scales, uint8_t* out_codes, uint8_t* out_scales,
+                          cudaStream_t stream);
 // pdl: launch with programmatic stream serialization (see pdl_attribute)
 cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
                           int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream,

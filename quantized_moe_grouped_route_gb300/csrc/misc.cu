@@ -36,8 +36,13 @@ __global__ void repack_codes_kernel(const uint8_t* __restrict__ w, int E, int N,
   }
 }
 
+// swz: the input scales are in the 128x4 swizzle of CUTLASS / FlashInfer NVFP4 weights
+// (megamoe_rm.cu page, scale_off): per expert, tiles of 128 rows x 4 scales, 512 bytes
+// each, the 4-column tile index fastest; inside a tile, row r's 4 scales at
+// (r % 32) * 16 + ((r / 32) % 4) * 4.  A row's 8 scales of one 128-wide K block are
+// then two 4-byte words, 512 bytes apart.
 __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N, int K, int w13,
-                                     uint2* __restrict__ out) {
+                                     int swz, uint2* __restrict__ out) {
   const int nrb = N / 128, nks = K / 128;
   const long long total = (long long)E * N * nks;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -49,7 +54,18 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N
     const int rb = (int)(rest % nrb);
     const int e = (int)(rest / nrb);
     const int n = repack_row(w13 != 0, N, rb, r);
-    out[idx] = *reinterpret_cast<const uint2*>(s + ((size_t)e * N + n) * (size_t)(K / 16) + ks * 8);
+    const size_t C = (size_t)(K / 16);
+    if (swz) {
+      const uint8_t* se = s + (size_t)e * N * C;
+      const size_t o = ((size_t)(n >> 7) * (C >> 2) + (size_t)ks * 2) * 512 + (size_t)(n & 31) * 16 +
+                       (size_t)((n >> 5) & 3) * 4;
+      uint2 v;
+      v.x = *reinterpret_cast<const uint32_t*>(se + o);
+      v.y = *reinterpret_cast<const uint32_t*>(se + o + 512);
+      out[idx] = v;
+    } else {
+      out[idx] = *reinterpret_cast<const uint2*>(s + ((size_t)e * N + n) * C + ks * 8);
+    }
   }
 }
 
@@ -163,7 +179,8 @@ int grid_for(long long work, int threads, int num_sms) {
 }  // namespace
 
 cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
-                          uint8_t* out_codes, uint8_t* out_scales, cudaStream_t stream) {
+                          bool swizzled_scales, uint8_t* out_codes, uint8_t* out_scales,
+                          cudaStream_t stream) {
   const long long words = (long long)E * N * (K / 8);
   const long long rows = (long long)E * N * (K / 128);
   repack_codes_kernel<<<grid_for(words, 256, 1184), 256, 0, stream>>>(
@@ -171,7 +188,7 @@ cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int 
   cudaError_t rc = cudaGetLastError();
   if (rc != cudaSuccess) return rc;
   repack_scales_kernel<<<grid_for(rows, 256, 1184), 256, 0, stream>>>(
-      s, E, N, K, w13 ? 1 : 0, reinterpret_cast<uint2*>(out_scales));
+      s, E, N, K, w13 ? 1 : 0, swizzled_scales ? 1 : 0, reinterpret_cast<uint2*>(out_scales));
   return cudaGetLastError();
 }
 

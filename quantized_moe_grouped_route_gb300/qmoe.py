@@ -34,6 +34,8 @@ QMOE_SCHED_PREFILL = 2
 QMOE_SCHED_PREFILL_PAIR = 3
 QMOE_W13 = 1
 QMOE_W2 = 2
+QMOE_SCALES_PLAIN = 0
+QMOE_SCALES_SWIZZLED_128X4 = 1
 
 _ERRORS = {QMOE_ERR_ARG: "argument", QMOE_ERR_SHAPE: "shape", QMOE_ERR_CUDA: "cuda",
            QMOE_ERR_TIMEOUT: "timeout", QMOE_ERR_ARCH: "arch", QMOE_ERR_WORKSPACE: "workspace",
@@ -70,6 +72,7 @@ def _bind(L):
         "qmoe_repacked_fp4_size": (sz, [i32, i32, i32]),
         "qmoe_repacked_scale_size": (sz, [i32, i32, i32]),
         "moe_nvfp4_repack": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
+        "moe_nvfp4_repack_layout": (i32, [P, P, i32, i32, i32, i32, i32, P, P, P]),
         "qmoe_forward_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "moe_nvfp4_forward": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P,
                                     sz, P]),
@@ -200,19 +203,24 @@ def moe_route(topk_ids: torch.Tensor, E: int, tile_n: int, stream=None):
     return offsets, sorted_pair[:P], pair_pos[:P], tiles, n_tiles, ws
 
 
-def moe_nvfp4_repack(w_fp4: torch.Tensor, w_scale: torch.Tensor, which: int, stream=None):
-    """Plain [E][N][K/2] codes + [E][N][K/16] scales -> repacked (codes, scales)."""
+def moe_nvfp4_repack(w_fp4: torch.Tensor, w_scale: torch.Tensor, which: int, stream=None,
+                     scale_layout: int = QMOE_SCALES_PLAIN):
+    """Plain [E][N][K/2] codes + block scales -> repacked (codes, scales).  Scales are
+    [E][N][K/16] (QMOE_SCALES_PLAIN) or, with QMOE_SCALES_SWIZZLED_128X4, N*K/16 bytes
+    per expert in the 128x4 swizzle of CUTLASS / FlashInfer checkpoints."""
     _need(w_fp4, torch.uint8, "w_fp4")
     _need(w_scale, torch.uint8, "w_scale")
     E, N, K2 = w_fp4.shape
     K = 2 * K2
-    if tuple(w_scale.shape) != (E, N, K // 16):
+    if w_scale.numel() != E * N * (K // 16) or w_scale.shape[0] != E:
         raise ValueError("w_scale shape does not match w_fp4")
+    if scale_layout == QMOE_SCALES_PLAIN and tuple(w_scale.shape) != (E, N, K // 16):
+        raise ValueError("plain w_scale must be [E][N][K/16]")
     codes = torch.empty(qmoe_repacked_fp4_size(E, N, K), dtype=torch.uint8, device=w_fp4.device)
     scales = torch.empty(qmoe_repacked_scale_size(E, N, K), dtype=torch.uint8, device=w_fp4.device)
-    rc = lib().moe_nvfp4_repack(_ptr(w_fp4), _ptr(w_scale), E, N, K, which, _ptr(codes),
-                                _ptr(scales), _stream(stream))
-    _check("moe_nvfp4_repack", rc)
+    rc = lib().moe_nvfp4_repack_layout(_ptr(w_fp4), _ptr(w_scale), E, N, K, which, scale_layout,
+                                       _ptr(codes), _ptr(scales), _stream(stream))
+    _check("moe_nvfp4_repack_layout", rc)
     return codes, scales
 
 
@@ -312,11 +320,11 @@ def qmoe_selftest_timeout(limit_ns: int, device="cuda", stream=None) -> int:
 class NVFP4MoE:
     """One MoE layer's repacked NVFP4 weights plus a reusable workspace."""
 
-    def __init__(self, w13, s13, gs13, w2, s2, gs2, stream=None):
+    def __init__(self, w13, s13, gs13, w2, s2, gs2, stream=None, scale_layout=QMOE_SCALES_PLAIN):
         E, N13, H2 = w13.shape
         self.E, self.I, self.H = E, N13 // 2, 2 * H2
-        self.w13c, self.w13s = moe_nvfp4_repack(w13, s13, QMOE_W13, stream)
-        self.w2c, self.w2s = moe_nvfp4_repack(w2, s2, QMOE_W2, stream)
+        self.w13c, self.w13s = moe_nvfp4_repack(w13, s13, QMOE_W13, stream, scale_layout)
+        self.w2c, self.w2s = moe_nvfp4_repack(w2, s2, QMOE_W2, stream, scale_layout)
         self.gs13 = gs13.contiguous()
         self.gs2 = gs2.contiguous()
         self._ws = None

@@ -77,6 +77,13 @@ def test_bad_arguments_are_rejected_before_any_device_work(lib):
         rc = lib.moe_nvfp4_forward_limit(null, null, null, null, null, null, null, null, null,
                                          null, 0, 128, 128, 8, 2, 0, good, null, 0, null)
         assert rc == qmoe.QMOE_OK
+    # repack with a scale layout: unknown layout, then the same checks as the plain call
+    assert lib.moe_nvfp4_repack_layout(null, null, 1, 128, 128, 1, 2, null, null, null) == \
+        qmoe.QMOE_ERR_ARG
+    assert lib.moe_nvfp4_repack_layout(null, null, 1, 100, 128, 1, 1, null, null, null) == \
+        qmoe.QMOE_ERR_SHAPE
+    assert lib.moe_nvfp4_repack_layout(null, null, 1, 128, 128, 1, 1, null, null, null) == \
+        qmoe.QMOE_ERR_ARG
     # repack: bad role, bad shape
     assert lib.moe_nvfp4_repack(null, null, 1, 128, 128, 3, null, null, null) == qmoe.QMOE_ERR_ARG
     assert lib.moe_nvfp4_repack(null, null, 1, 100, 128, 1, null, null, null) == qmoe.QMOE_ERR_SHAPE
