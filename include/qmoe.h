@@ -150,6 +150,9 @@ int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E
  * sharing one workspace must not overlap on the GPU.
  */
 size_t qmoe_forward_workspace_size(int M, int H, int I, int E, int top_k, int sched);
+/* Kernels one moe_nvfp4_forward call launches (route, gather, FC1, FC2, combine; the
+ * route is three kernels above 8192 pairs); 0 for M = 0, QMOE_ERR_ARG for bad sizes. */
+int qmoe_forward_kernel_count(int M, int top_k, int E, int sched);
 int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8_t* w13_scale_dev,
                       const float* w13_gscale_dev, const uint8_t* w2_fp4_dev,
                       const uint8_t* w2_scale_dev, const float* w2_gscale_dev,

@@ -153,6 +153,14 @@ int qmoe_sched_tile_n(int sched, int M, int top_k, int E) {
   return gemm_tile_n(resolve_sched(sched, M, top_k, E));
 }
 
+int qmoe_forward_kernel_count(int M, int top_k, int E, int sched) {
+  if (M < 0 || top_k < 1 || E < 1) return QMOE_ERR_ARG;
+  if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
+  if (M == 0) return 0;
+  const long long P = (long long)M * top_k;
+  return 4 + (route_scratch_bytes(P, E) > 0 ? 3 : 1);
+}
+
 int qmoe_max_tiles(int M, int top_k, int E, int tile_n) {
   if (M < 0 || top_k < 1 || E < 1 || tile_n < 1) return QMOE_ERR_ARG;
   const long long P = (long long)M * top_k;

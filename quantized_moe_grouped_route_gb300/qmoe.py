@@ -67,6 +67,7 @@ def _bind(L):
     sig = {
         "qmoe_sched_tile_n": (i32, [i32, i32, i32, i32]),
         "qmoe_max_tiles": (i32, [i32, i32, i32, i32]),
+        "qmoe_forward_kernel_count": (i32, [i32, i32, i32, i32]),
         "qmoe_route_workspace_size": (sz, [i32, i32, i32, i32]),
         "moe_route": (i32, [P, i32, i32, i32, i32, P, P, P, P, P, P, sz, P]),
         "qmoe_repacked_fp4_size": (sz, [i32, i32, i32]),
@@ -126,6 +127,10 @@ def _need(t: torch.Tensor, dtype, name: str):
 # --------------------------------------------------------------------- sizes
 def qmoe_sched_tile_n(sched: int, M: int, top_k: int, E: int) -> int:
     return lib().qmoe_sched_tile_n(sched, M, top_k, E)
+
+
+def qmoe_forward_kernel_count(M: int, top_k: int, E: int, sched: int = QMOE_SCHED_AUTO) -> int:
+    return lib().qmoe_forward_kernel_count(M, top_k, E, sched)
 
 
 def qmoe_max_tiles(M: int, top_k: int, E: int, tile_n: int) -> int:

@@ -35,6 +35,11 @@ def test_size_queries(lib):
     # above 8192 pairs the route keeps per-warp count tables in its workspace
     assert qmoe.qmoe_route_workspace_size(1024, 8, 256, 320) == 256
     assert qmoe.qmoe_route_workspace_size(8192, 8, 256, 320) == 256 + 16 * 16 * 256 * 4
+    # kernels per forward: route (one, or three above 8192 pairs), gather, FC1, FC2, combine
+    assert qmoe.qmoe_forward_kernel_count(16, 8, 256, qmoe.QMOE_SCHED_AUTO) == 5
+    assert qmoe.qmoe_forward_kernel_count(8192, 8, 256, qmoe.QMOE_SCHED_AUTO) == 7
+    assert qmoe.qmoe_forward_kernel_count(0, 8, 256, qmoe.QMOE_SCHED_AUTO) == 0
+    assert qmoe.qmoe_forward_kernel_count(4, 0, 8, qmoe.QMOE_SCHED_AUTO) == qmoe.QMOE_ERR_ARG
     assert qmoe.qmoe_repacked_fp4_size(256, 4096, 7168) == 256 * 4096 * 3584
     assert qmoe.qmoe_repacked_scale_size(256, 7168, 2048) == 256 * 7168 * 128
     ws = qmoe.qmoe_forward_workspace_size(8192, 7168, 2048, 256, 8)
