@@ -45,7 +45,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 [rows][cols] operand, boxes of 64 columns x 16 rows, 128-byte swizzle.
 // Tensor map over a row-major bf16 matrix [rows][cols] for the GEMM's pair rows.
 // box_slabs == 0: 2-D, box box_rows rows x 64 elements.  box_slabs > 0: 3-D view
 // {64 elements, rows, cols / 64 slabs} (slab stride 128 bytes), box

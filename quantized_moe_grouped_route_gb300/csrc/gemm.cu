@@ -3,11 +3,13 @@
 //
 // What it computes (megamoe_rm.cu page, fc1_rm / fc2_rm; spec layer):
 //   FC1 tile (expert e, 128 weight rows rb, pair tile t):
-//     g = gs13[e] * Wq13[e][rows] . xs[t]^T, then h = bf16(SiLU(gate) * up)
+//     g = gs13[e] * Wq13[e][rows] . xs[t]^T, then h = bf16(SiLU(gate) * up), with
+//     the GLM clamp of gate and up first when a SwiGLU limit is given (CLAMP)
 //   FC2 tile: y = gs2[e] * Wq2[e][rows] . h[t]^T, ypart[pair][j] = topk_w[pair] * y
 // Each unit is one 128-row block of one expert's weights against one tile of that
 // expert's pairs (<= NMAX pairs) over the whole K: the weights are the MMA's M side
-// ("swap AB": weight rows on M = 128, pairs on N = 16..NMAX), so small per-expert
+// ("swap AB": weight rows on M = 128, pairs on N = 16..256; a wider tile as two
+// MMAs per K slice), so small per-expert
 // batches still fill the instruction, and every output element is produced by one
 // CTA in a fixed order (deterministic, no split reduction).
 //
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   using C = Cfg<NMAX, RS, SL, ACCB, DG, NMW, KS>;
   static_assert(BIN || KS == 1, "2-D pair-row boxes are issued per 128-wide block");
   // BIN: pair rows as one 3-D box {64, NMAX rows, 2 KS slabs} per step, copied by the
-  // MMA warps; otherwise 2-D boxes of 16 rows from a producer warp
+  // MMA warps; otherwise 2-D boxes of kPairBoxRows rows from a producer warp
   constexpr int kWeightTmaWarp = weight_tma_warp(BIN);
   constexpr int kPairTmaWarp = pair_tma_warp(BIN);
   extern __shared__ uint8_t smem_raw[];
