@@ -37,9 +37,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -67,10 +64,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's abort
@@ -134,15 +127,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
-// Contiguous global -> shared copy; dst, src 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
 
 __device__ __forceinline__ void bulk_g2s_if(uint32_t pred, uint32_t dst, const void* src, uint32_t bytes,
                                             uint32_t bar, uint64_t policy) {
@@ -176,15 +160,6 @@ __device__ __forceinline__ void tma_load_3d_if(uint32_t pred, uint32_t dst, cons
       : "memory");
 }
 
-// 2-D tiled tensor copy; x (innermost) must be a multiple of 8 bf16 elements.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -221,11 +196,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread
+// completes; issued only where pred != 0.
 __device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
@@ -234,7 +206,8 @@ __device__ __forceinline__ void tc_commit_if(uint32_t pred, uint32_t bar) {
       "r"(bar)
       : "memory");
 }
-// As mma_bf16_ts, issued only where pred != 0 (one elected lane of a converged warp).
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (bf16 inputs, fp32 accumulate), issued
+// only where pred != 0 (one elected lane of a converged warp).
 __device__ __forceinline__ void mma_bf16_ts_if(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,
                                                uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate) {
@@ -324,16 +297,6 @@ __device__ __forceinline__ void mma_bf16_ts_slab4x2(uint32_t pred, uint32_t d0, 
   }
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
@@ -393,6 +356,5 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
 }  // namespace qmoe
