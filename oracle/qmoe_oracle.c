@@ -217,16 +217,22 @@ static void bf16_bracket(double v, double* lo, double* hi) {
  * such decisions from the caller: h_given ([n_tokens * top_k][I] bf16 bits, row
  * t * top_k + k for the t-th listed token) replaces the oracle's own rounding, after
  * each given value is checked to be a valid rounding: the bf16 rounding of some value
- * within delta of the exact silu(gate) * up, where delta is the first-order effect of
- * fp32 accumulation errors on the two dot products,
- *   d_up   = c * u * gs13 * sum_h |x[h] * Wq13[i][h]|        (likewise d_gate, row I+i)
- *   delta  = |silu(gate)| * d_up + 1.1 * |up| * d_gate + 8 * u * |silu(gate) * up|
- * with u = 2^-24 (fp32 unit roundoff), c = 2 * (H / 16 + 4) (one rounding per
- * 16-wide MMA step of the accumulation, doubled), 1.1 >= max |SiLU'|.  h_stats (may
- * be NULL) receives {values compared, values that differ from the oracle's own
- * rounding, values that are not a valid rounding}.  h_out (may be
- * NULL, same layout as h_given) receives the h values used; rows of slots without an
- * expert are zero.
+ * within delta of the exact silu(gate) * up.  delta is the first-order error of an
+ * fp32 evaluation in which the dot product is accumulated as a tensor core does it:
+ * the products x[h] * Wq[n][h] are exact, each 16-wide K slice sum S_s is rounded to
+ * fp32 and added to an fp32 running sum P_s (P_s = S_0 + .. + S_s), every rounding
+ * with relative error at most 2u, u = 2^-24 (so both round-to-nearest and truncation
+ * are covered):
+ *   e_dot  = 2u * (sum_s |S_s| + sum_s |P_s|)
+ *   d_up   = |gs13| * e_dot(row i)   + u * |up|       (the global-scale product rounded)
+ *   d_gate = |gs13| * e_dot(row I+i) + u * |gate|
+ *   delta  = |silu(gate)| * d_up + 1.1 * (|up| + d_up) * d_gate + 8 * u * |silu(gate) * up|
+ * since |SiLU(g + e) - SiLU(g)| <= 1.1 |e| (1.1 >= max |SiLU'|), the product's error is
+ * at most |silu(gate)| d_up + 1.1 d_gate (|up| + d_up); the last term covers the fp32
+ * SiLU and product.  h_stats
+ * (may be NULL) receives {values compared, values that differ from the oracle's own
+ * rounding, values that are not a valid rounding}.  h_out (may be NULL, same layout
+ * as h_given) receives the h values used; rows of slots without an expert are zero.
  */
 /* As qo_forward_h, with the SwiGLU limit swiglu_limit (> 0; +infinity: no clamp)
  * applied to gate and up before h (fc1_rm epilogue, GLM variant).  The clamps are
@@ -253,7 +259,7 @@ int qo_forward_hl(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, con
     double* ga = (double*)malloc(sizeof(double) * (size_t)(2 * I));
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
     double* acc = (double*)malloc(sizeof(double) * (size_t)H);
-    const double u = ldexp(1.0, -24), c_acc = 2.0 * (double)(H / 16 + 4);
+    const double u = ldexp(1.0, -24);
 #pragma omp for schedule(dynamic, 1)
     for (int64_t t = 0; t < n_tokens; ++t) {
       int64_t m = tokens ? tokens[t] : t;
@@ -270,14 +276,18 @@ int qo_forward_hl(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, con
         const uint8_t* we = w13 + (int64_t)e * (2 * I) * (H / 2);
         const uint8_t* se = s13 + (int64_t)e * (2 * I) * (H / 16);
         for (int64_t n = 0; n < 2 * I; ++n) {
-          double sum = 0.0, asum = 0.0;
+          double sum = 0.0, slice = 0.0, err = 0.0;
           for (int64_t hh = 0; hh < H; ++hh) {
             double term = qo_bf16_to_double(x[m * H + hh]) * wq(we, se, H, n, hh);
             sum += term;
-            asum += fabs(term);
+            slice += term;
+            if (hh % 16 == 15) { /* a 16-wide K slice ends: its sum and the running sum */
+              err += fabs(slice) + fabs(sum);
+              slice = 0.0;
+            }
           }
           g[n] = (double)gs13[e] * sum;
-          ga[n] = fabs((double)gs13[e]) * asum;
+          ga[n] = fabs((double)gs13[e]) * 2.0 * u * err;
         }
         for (int64_t i = 0; i < I; ++i) {
           double up = g[i], gate = g[I + i];
@@ -289,7 +299,8 @@ int qo_forward_hl(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, con
           h[i] = qo_bf16_to_double(qo_bf16_rne(exact));
           if (h_given) {
             double given = qo_bf16_to_double(h_given[(t * top_k + k) * I + i]);
-            double delta = fabs(silu) * c_acc * u * ga[i] + 1.1 * fabs(up) * c_acc * u * ga[I + i] +
+            double d_up = ga[i] + u * fabs(up), d_gate = ga[I + i] + u * fabs(gate);
+            double delta = fabs(silu) * d_up + 1.1 * (fabs(up) + d_up) * d_gate +
                            8.0 * u * fabs(exact);
             double lo, hi, lo2, hi2;
             bf16_bracket(exact - delta, &lo, &hi2);

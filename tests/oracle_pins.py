@@ -303,6 +303,139 @@ def pin_h_given(lib):
         assert st["outside"] == 1
 
 
+# ---------------------------------------------------------------------------
+# the h-acceptance bound at production size, against emulated fp32 accumulation
+# ---------------------------------------------------------------------------
+
+EMU_SLICE = 16    # K per tcgen05 MMA of kind::f16
+EMU_STEP = 256    # K per pipeline step of the decode schedule (its MMA warps alternate)
+
+
+def _round32(v64, truncate):
+    """float64 -> float32, to nearest (ties to even) or toward zero."""
+    t = v64.astype(np.float32)
+    if truncate:
+        over = np.abs(t.astype(np.float64)) > np.abs(v64)
+        t = np.where(over, np.nextafter(t, np.float32(0)), t)
+    return t
+
+
+def _add32(a, b, truncate):
+    # the sum of two float32 values is exact in float64 at the magnitudes met here
+    return _round32(a.astype(np.float64) + b.astype(np.float64), truncate)
+
+
+def emulate_fc1_h(x, w13, gs, chains, truncate):
+    """bf16 bits of h = SiLU(gate) * up as the grouped GEMM forms them, emulated:
+    x [M][H] bf16 values and w13 [2I][H] exact dequantized weights (float64); products
+    exact, each 16-wide K slice sum rounded to fp32 and added to an fp32 accumulator,
+    the 256-wide K steps dealt round robin over `chains` accumulators which are added
+    in order at the end; every rounding to nearest or toward zero (`truncate`); then
+    the global scale, SiLU and the product in fp32 and a round to bf16."""
+    M, H = x.shape
+    N = w13.shape[0]
+    ns = H // EMU_SLICE
+    xs = x.reshape(M, ns, EMU_SLICE).transpose(1, 0, 2)
+    ws = w13.reshape(N, ns, EMU_SLICE).transpose(1, 2, 0)
+    slices = np.matmul(xs, ws)                               # [slice][m][n], fp64
+    acc = np.zeros((chains, M, N), np.float32)
+    per_step = EMU_STEP // EMU_SLICE
+    for s_ in range(ns):
+        c = (s_ // per_step) % chains
+        acc[c] = _add32(acc[c], _round32(slices[s_], truncate), truncate)
+    v = np.zeros((M, N), np.float32)
+    for c in range(chains):
+        v = _add32(v, acc[c], truncate)
+    g = _round32(v.astype(np.float64) * np.float64(np.float32(gs)), False)
+    I = N // 2
+    up, gate = g[:, :I], g[:, I:]
+    with np.errstate(over="ignore"):
+        e = np.exp(-gate).astype(np.float32)
+    h32 = ((gate / (np.float32(1) + e)).astype(np.float32) * up).astype(np.float32)
+    return torch.from_numpy(np.ascontiguousarray(h32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().astype(np.uint16)
+
+
+def h_bound_layer(M, I, seed=101, H=7168):
+    """One expert, one slot per token: the h-given statistics of each token's h."""
+    from qmoe_inputs import LayerConfig, make_inputs
+    from oracle import ref_numpy
+    li = make_inputs(LayerConfig(f"hbound_m{M}_h{H}_i{I}", M, H, I, 1, 1, seed=seed), "cpu")
+    li.topk_weights = torch.ones_like(li.topk_weights)
+    x = oracle.bf16_bits_to_float(li.x.view(torch.int16).numpy().astype(np.uint16))
+    w13 = ref_numpy.dequant(li.w13[0].numpy(), li.s13[0].numpy())
+    return li, x, w13, float(li.gs13[0])
+
+
+def h_given_stats(lib, li, hg):
+    _, st = oracle.forward(li.x, li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2, li.topk_ids,
+                           li.topk_weights, h_given=hg, lib=lib)
+    return st
+
+
+def two_steps_away(own, direction):
+    """bf16 bits moved `direction` (+2 / -2) steps in magnitude; tiny and huge values kept."""
+    mag = own & 0x7FFF
+    ok = (mag >= 4) & (mag < 0x7F00)
+    far = np.where(ok, own.astype(np.int32) + direction, own.astype(np.int32)).astype(np.uint16)
+    return far, int(ok.sum())
+
+
+def cancelling_layer(M, I, seed=103, H=7168):
+    """h_bound_layer whose dot products cancel: the second half of K repeats the first
+    half of x with every weight's sign flipped (same scales), and one activation of the
+    second half is perturbed, so the exact g is small while the running sums of the
+    accumulation are not: the fp32 error then spans many bf16 steps of h."""
+    li, x, w13, gs = h_bound_layer(M, I, seed=seed, H=H)
+    half = H // 2
+    w = li.w13[0].numpy()
+    w[:, half // 2:] = w[:, : half // 2] ^ 0x88          # both nibbles' sign bits
+    sc = li.s13[0].numpy()
+    sc[:, half // 16:] = sc[:, : half // 16]
+    xb = li.x.view(torch.int16).numpy()
+    xb[:, half:] = xb[:, :half]
+    xb[:, H - 1] = np.int16(0x3F80)                       # 1.0
+    from oracle import ref_numpy
+    x = oracle.bf16_bits_to_float(xb.astype(np.uint16))
+    w13 = ref_numpy.dequant(w, sc)
+    return li, x, w13, gs
+
+
+_HB = None
+_HC = None
+
+
+def pin_h_bound_production(lib):
+    """At H = 7168 every emulated fp32 accumulation (one or three accumulators, rounding
+    to nearest or truncating) is accepted, and values two bf16 steps from the oracle's
+    own rounding are rejected except where the exact value's error bound is that wide
+    (cancelling dot products: under 2% here)."""
+    global _HB
+    if _HB is None:
+        _HB = h_bound_layer(16, 256)
+    li, x, w13, gs = _HB
+    for chains, trunc in ((1, True), (3, True), (1, False)):
+        st = h_given_stats(lib, li, emulate_fc1_h(x, w13, gs, chains, trunc))
+        assert st["compared"] == 16 * 256 and st["outside"] == 0, (chains, trunc, st)
+    own = oracle.forward(li.x, li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2, li.topk_ids,
+                         li.topk_weights, return_h=True, lib=lib)[1]["h"]
+    for d in (2, -2):
+        far, moved = two_steps_away(own, d)
+        st = h_given_stats(lib, li, far)
+        assert moved - st["outside"] <= 0.02 * moved, (d, moved, st)
+    # cancelling dot products: the emulated accumulations land several bf16 steps from
+    # the exact value, where only the running-sum part of the bound admits them
+    global _HC
+    if _HC is None:
+        _HC = cancelling_layer(16, 128)
+    li, x, w13, gs = _HC
+    for chains, trunc in ((1, True), (3, True), (1, False)):
+        st = h_given_stats(lib, li, emulate_fc1_h(x, w13, gs, chains, trunc))
+        assert st["outside"] == 0, (chains, trunc, st)
+        if trunc:
+            assert st["flipped"] >= st["compared"] // 8, st
+
+
 def pin_permutation_blocks(lib):
     """Permutation-matrix weights: up[i] = x[sig(i)], gate[i] = 2 x[tau(i)],
     out[j] = h[pi(j)] with h = bf16(silu(gate) * up)."""
@@ -513,6 +646,6 @@ def pin_swiglu_limit_numpy_twin(lib):
 
 
 ALL_PINS = [pin_e2m1, pin_e4m3, pin_bf16_decode, pin_bf16_round, pin_route, pin_zero_weights,
-            pin_single_nibble, pin_h_given, pin_permutation_blocks, pin_subnormal_scale, pin_token_permutation,
+            pin_single_nibble, pin_h_given, pin_h_bound_production, pin_permutation_blocks, pin_subnormal_scale, pin_token_permutation,
             pin_duplicate_expert, pin_weight_linearity, pin_numpy_twin, pin_tiny_config,
             pin_swiglu_limit, pin_swiglu_limit_infinite, pin_swiglu_limit_numpy_twin]

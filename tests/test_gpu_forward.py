@@ -9,7 +9,7 @@ import torch
 
 from quantized_moe_grouped_route_gb300 import qmoe
 from qmoe_inputs import CONFIGS, LayerConfig, make_inputs
-from tests.helpers import check_layer, gpu_forward
+from tests.helpers import check_layer, forced_tokens, gpu_forward
 
 pytestmark = pytest.mark.gpu
 
@@ -64,22 +64,17 @@ def test_duplicate_experts_and_bad_ids():
     check_layer(li, out, layer._ws, qmoe.QMOE_SCHED_AUTO, what="duplicates")
 
 
-def _sample_tokens(M, n, seed):
-    if M <= n:
-        return np.arange(M)
-    rng = np.random.default_rng(seed)
-    s = np.sort(rng.choice(M, size=n - 2, replace=False))
-    return np.unique(np.concatenate([[0, M - 1], s]))
-
-
 @pytest.mark.parametrize("cfg", CONFIGS[1:], ids=lambda c: c.name)
 def test_full_config_sampled_tokens(cfg):
+    """The benchmark's launch configuration on each full workload: 64 random tokens plus
+    the tokens of the heaviest expert's tail tile, of the lightest experts and of the
+    second MMA chain of wide tiles, against the unconditioned oracle (check_layer)."""
     li = make_inputs(cfg, "cuda")
     torch.cuda.synchronize()
     out, layer = gpu_forward(li, qmoe.QMOE_SCHED_AUTO)
     rc, flags = qmoe.qmoe_read_error(layer._ws)
     assert rc == 0 and flags == 0
-    toks = _sample_tokens(cfg.M, 24, cfg.seed)
+    toks = forced_tokens(li, qmoe.QMOE_SCHED_AUTO, n_random=64, seed=cfg.seed)
     check_layer(li, out, layer._ws, qmoe.QMOE_SCHED_AUTO, tokens=toks, what=cfg.name)
     # deterministic: a second call is bitwise equal
     out2, _ = gpu_forward(li, qmoe.QMOE_SCHED_AUTO, layer)

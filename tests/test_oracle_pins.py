@@ -36,6 +36,10 @@ MUTANTS = {
     "h_not_rounded": ("h[i] = qo_bf16_to_double(qo_bf16_rne(exact));", "h[i] = exact;"),
     "h_given_ignored": ("            h[i] = given;\n", "\n"),
     "h_bracket_one_sided": ("if (!(given >= lo && given <= hi)) n_out += 1;", "if (!(given >= lo)) n_out += 1;"),
+    "h_bound_no_running_sum": ("err += fabs(slice) + fabs(sum);", "err += fabs(slice);"),
+    "h_bound_worst_case_wide": ("ga[n] = fabs((double)gs13[e]) * 2.0 * u * err;",
+                                "ga[n] = fabs((double)gs13[e]) * 2.0 * u * err * 200.0;"),
+    "h_bound_first_order_only": ("1.1 * (fabs(up) + d_up) * d_gate", "1.1 * fabs(up) * d_gate"),
     "h_flip_uncounted": ("if (given != h[i]) n_flip += 1;", ";"),
     "routing_weight_dropped": ("acc[j] += (double)topk_w[m * top_k + k] * y;", "acc[j] += y;"),
     "e2m1_sign_dropped": ("return (code & 8) ? -m : m;", "return m;"),

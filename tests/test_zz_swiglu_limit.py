@@ -10,7 +10,7 @@ import torch
 
 from quantized_moe_grouped_route_gb300 import qmoe
 from qmoe_inputs import CONFIGS, LayerConfig, make_inputs
-from tests.helpers import check_layer, gpu_forward, oracle_forward
+from tests.helpers import check_layer, forced_tokens, gpu_forward
 
 pytestmark = pytest.mark.gpu
 
@@ -57,8 +57,7 @@ def test_full_configs_with_limit_sampled_tokens(cfg):
     out, layer = gpu_forward(li, qmoe.QMOE_SCHED_AUTO, swiglu_limit=limit)
     rc, flags = qmoe.qmoe_read_error(layer._ws)
     assert rc == 0 and flags == 0
-    rng = np.random.default_rng(cfg.seed)
-    toks = np.unique(np.concatenate([[0, cfg.M - 1], rng.choice(cfg.M, 14, replace=False)]))
+    toks = forced_tokens(li, qmoe.QMOE_SCHED_AUTO, n_random=32, seed=cfg.seed)
     check_layer(li, out, layer._ws, qmoe.QMOE_SCHED_AUTO, tokens=toks,
                 what=f"{cfg.name} limit={limit}", swiglu_limit=limit)
     # deterministic
