@@ -16,7 +16,7 @@
  *  - Pointers named *_dev are device pointers owned by the caller; the library
  *    never allocates, frees or keeps them.  `stream` is a cudaStream_t (may be
  *    NULL for the legacy default stream); all work is enqueued on it and no call
- *    synchronises the host, except qmoe_read_error.
+ *    synchronises the host, except qmoe_read_error and qmoe_noalloc_read_error.
  *  - Every call returns QMOE_OK (0) or a negative QMOE_ERR_* code and never
  *    throws or aborts.  Argument checks run before anything is enqueued.
  *  - Shapes: H % 128 == 0, I % 128 == 0, 1 <= E <= 2048, 1 <= top_k <= 64,
@@ -108,7 +108,7 @@ int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
  * N % 128 == 0 and K % 128 == 0 are required (QMOE_ERR_SHAPE otherwise).
  */
 /*
- * moe_nvfp4_repack_layout — moe_nvfp4_repack taking the block scales in one of two
+ * moe_nvfp4_repack_layout — moe_nvfp4_repack taking the block scales in one of three
  * layouts (output identical for the same scale values):
  *   QMOE_SCALES_PLAIN          [E][N][K/16], row-major (as moe_nvfp4_repack)
  *   QMOE_SCALES_SWIZZLED_128X4 per expert N*K/16 bytes in the 128x4 swizzle that
@@ -116,10 +116,16 @@ int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
  *       tiles of 128 rows x 4 scales, 512 bytes each, the 4-column tile index
  *       fastest; inside a tile the scale of row r, column c at
  *       (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4.
+ *   QMOE_SCALES_PACKED_U32     uint32 [E][N][K/64], four UE4M3 scales per word
+ *       (tilelang_kernels.py page, grouped_gemm_fp4_packed_sf): the scale of K block
+ *       4g + j in bits 8j..8j+7 of word g (the page gives no byte order; this is the
+ *       order of a little-endian uint32 view of the plain bytes).  w_scale_dev must be
+ *       4-byte aligned (16-byte, as for every pointer here).
  * Other arguments and errors as moe_nvfp4_repack; an unknown layout: QMOE_ERR_ARG.
  */
 #define QMOE_SCALES_PLAIN 0
 #define QMOE_SCALES_SWIZZLED_128X4 1
+#define QMOE_SCALES_PACKED_U32 2
 int moe_nvfp4_repack_layout(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N,
                             int K, int which, int scale_layout, uint8_t* out_fp4_dev,
                             uint8_t* out_scale_dev, void* stream);
@@ -189,15 +195,19 @@ int moe_nvfp4_forward_limit(const void* x_dev, const uint8_t* w13_fp4_dev,
  *    M, H, I, E, top_k, sched) <= QMOE_NOALLOC_SCRATCH_BYTES (decode-sized batches:
  *    e.g. M = 16, H = 7168, I = 2048, top_k = 8 needs about 6 MB); larger batches get
  *    QMOE_ERR_WORKSPACE before anything is enqueued.
- *  - Set-up: the first call on a device, made with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call before any
- *    stream capture.
+ *  - Set-up: the array's device address is looked up (cudaGetSymbolAddress) on the
+ *    first call made on a device, and again whenever a call finds another CUDA context
+ *    current than the one of the last lookup (after cudaDeviceReset, or when the caller
+ *    runs its own context); it is the address in the context current at the call.  A
+ *    lookup makes the device's primary context current if the thread had none.  Make
+ *    the first call on a device, and the first call in a new context, before any stream
+ *    capture.  The lookup is guarded by a lock, so threads may make first calls at once.
  *  - It calls no cudaMalloc / cudaFree and no allocating library routine.
  *  - Every call shares the one array and leaves its contents behind; the error word
  *    in it is cleared at the start of each call.  Calls that overlap on the GPU (on
  *    different streams, or from several host threads) race on the array and give
- *    wrong results: serialise them.  qmoe_read_error cannot see this array; a
- *    bad-id or timeout flag from this call is not reported.
+ *    wrong results: serialise them.  qmoe_noalloc_read_error reads the error word
+ *    (bad expert ids, expired waits) of the last call.
  * The pages have no counterpart of this entry point.
  */
 #define QMOE_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -207,6 +217,14 @@ int moe_nvfp4_forward_noalloc(const void* x_dev, const uint8_t* w13_fp4_dev,
                               const float* w2_gscale_dev, const int32_t* topk_ids_dev,
                               const float* topk_weights_dev, void* out_dev, int M, int H, int I,
                               int E, int top_k, int sched, void* stream);
+
+/*
+ * qmoe_noalloc_read_error — qmoe_read_error for moe_nvfp4_forward_noalloc: copies the
+ * error word of the built-in scratch array (current device and context) to the host
+ * after the stream's work so far; synchronises `stream`.  Same flags and return codes
+ * as qmoe_read_error.  (No counterpart on the pages.)
+ */
+int qmoe_noalloc_read_error(void* stream, uint32_t* flags_out);
 
 /*
  * qmoe_forward_workspace_layout — byte offsets, inside a forward workspace, of what

@@ -5,6 +5,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -12,36 +15,50 @@ namespace qmoe {
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_num_sms[kMaxDevices];
-int g_arch_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 unsupported
+// Per-device facts looked up once (0 = not yet known); atomics, since several host
+// threads may make their first calls at the same time.
+std::atomic<int> g_num_sms[kMaxDevices];
+std::atomic<int> g_arch_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 unsupported
 
 int device_info(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMOE_ERR_CUDA;
-  if (g_arch_ok[dev] == 0) {
+  int ok = g_arch_ok[dev].load(std::memory_order_acquire);
+  if (ok == 0) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QMOE_ERR_CUDA;
-    g_num_sms[dev] = sms;
-    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    g_num_sms[dev].store(sms, std::memory_order_relaxed);
+    ok = (major == 10 && minor == 3) ? 1 : -1;
+    g_arch_ok[dev].store(ok, std::memory_order_release);
   }
-  if (g_arch_ok[dev] < 0) return QMOE_ERR_ARCH;
-  *num_sms = g_num_sms[dev];
+  if (ok < 0) return QMOE_ERR_ARCH;
+  *num_sms = g_num_sms[dev].load(std::memory_order_relaxed);
   return QMOE_OK;
 }
 
+// Driver entry points, resolved once (a function-local static is initialised once even
+// when several threads get here first).
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(ptr);
+  return nullptr;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn =
+      driver_fn<PFN_cuTensorMapEncodeTiled_v12000>("cuTensorMapEncodeTiled");
+  return fn;
+}
+
+PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+  static const PFN_cuCtxGetCurrent_v4000 fn = driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent");
   return fn;
 }
 
@@ -78,6 +95,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct ForwardLayout {
   size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, route_scratch, xs, h, ypart, total;
+  // decode schedule: arrival counters of FC1 and FC2 (cleared with the error word by one
+  // memset: [0, clear_bytes)) and the partial accumulators of split units
+  size_t sk_cnt1, sk_cnt2, clear_bytes, sk_part;
   int rows;  // rows of xs / h (>= 16, multiple of 16)
   int tile_n, max_tiles;
 };
@@ -107,7 +127,16 @@ ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {
   L.tile_n = gemm_tile_n(resolve_sched(sched, M, top_k, E));
   L.max_tiles = (int)((P + L.tile_n - 1) / L.tile_n) + E;
   L.rows = (int)align_up((size_t)(P > 0 ? P : 1), 16);
+  const bool sk = resolve_sched(sched, M, top_k, E) == QMOE_SCHED_DECODE;
   size_t off = kWsHeaderBytes;
+  L.sk_cnt1 = off;
+  off += sk ? sk_cnt_bytes((long long)L.max_tiles * (2 * I / 128)) : 0;
+  L.sk_cnt2 = off;
+  off += sk ? sk_cnt_bytes((long long)L.max_tiles * (H / 128)) : 0;
+  L.clear_bytes = off;
+  off = align_up(off, 256);
+  L.sk_part = off;
+  off = align_up(off + (sk ? sk_part_bytes() : 0), 256);
   L.offsets = off;
   off = align_up(off + 4 * (size_t)(E + 1), 256);
   L.sorted_pair = off;
@@ -137,9 +166,40 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA; 
 // routing tables, gathered activations, h and per-pair partial outputs.  Every GPU
 // that loads the library holds it until the process exits.
 __device__ __align__(256) uint8_t g_noalloc_scratch[QMOE_NOALLOC_SCRATCH_BYTES];
-// Its device address per device, looked up on the first call made with that
-// device current (host code cannot use the symbol itself as a device pointer).
-void* g_noalloc_addr[kMaxDevices];
+
+// Its device address.  Host code cannot use the symbol itself as a device pointer: the
+// address is looked up with cudaGetSymbolAddress, which gives the address in the CUDA
+// context current at the time.  It is cached per device together with that context and
+// looked up again whenever the calling thread's current context differs (after
+// cudaDeviceReset, or for a caller running its own context), under a lock.
+struct NoallocAddr {
+  CUcontext ctx;
+  void* addr;
+};
+NoallocAddr g_noalloc_addr[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMOE_ERR_CUDA;
+  auto get_ctx = ctx_current_fn();
+  if (!get_ctx) return QMOE_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return QMOE_ERR_CUDA;  // null: no context current yet
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoallocAddr& c = g_noalloc_addr[dev];
+  if (!ctx || c.ctx != ctx || !c.addr) {
+    // the lookup makes the device's primary context current if the thread had none
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
+      return QMOE_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return QMOE_ERR_CUDA;
+    c.ctx = ctx;
+    c.addr = addr;
+  }
+  *out = c.addr;
+  return QMOE_OK;
+}
 
 }  // namespace
 }  // namespace qmoe
@@ -208,7 +268,8 @@ int moe_nvfp4_repack_layout(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev
                             int K, int which, int scale_layout, uint8_t* out_fp4_dev,
                             uint8_t* out_scale_dev, void* stream) {
   if (which != QMOE_W13 && which != QMOE_W2) return QMOE_ERR_ARG;
-  if (scale_layout != QMOE_SCALES_PLAIN && scale_layout != QMOE_SCALES_SWIZZLED_128X4)
+  if (scale_layout != QMOE_SCALES_PLAIN && scale_layout != QMOE_SCALES_SWIZZLED_128X4 &&
+      scale_layout != QMOE_SCALES_PACKED_U32)
     return QMOE_ERR_ARG;
   if (E < 1 || E > 2048 || N < 128 || K < 128 || N % 128 || K % 128 || N > 131072 || K > 65536)
     return QMOE_ERR_SHAPE;
@@ -219,9 +280,8 @@ int moe_nvfp4_repack_layout(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev
   int sms = 0;
   int rc = device_info(&sms);
   if (rc != QMOE_OK) return rc;
-  return cuda_rc(launch_repack(w_fp4_dev, w_scale_dev, E, N, K, which == QMOE_W13,
-                               scale_layout == QMOE_SCALES_SWIZZLED_128X4, out_fp4_dev,
-                               out_scale_dev, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_rc(launch_repack(w_fp4_dev, w_scale_dev, E, N, K, which == QMOE_W13, scale_layout,
+                               out_fp4_dev, out_scale_dev, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E, int N, int K,
@@ -262,6 +322,15 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   if (rc != QMOE_OK) return rc;
   const int rsched = resolve_sched(sched, M, top_k, E);
   const int P = M * top_k;
+  {
+    // the GEMMs count a CTA's K steps (decode: all units' steps) in 32 bits
+    const unsigned long long steps_cap = rsched == QMOE_SCHED_DECODE ? (1ull << 31)
+                                                                     : (unsigned long long)sms << 31;
+    const unsigned long long k1 = H / 128, k2 = I / 128;
+    if ((unsigned long long)L.max_tiles * (2 * I / 128) * k1 >= steps_cap ||
+        (unsigned long long)L.max_tiles * (H / 128) * k2 >= steps_cap)
+      return QMOE_ERR_SHAPE;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace_dev);
   unsigned int* err = reinterpret_cast<unsigned int*>(ws);
@@ -282,7 +351,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
   };
-  if (cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, L.clear_bytes, s) != cudaSuccess) return QMOE_ERR_CUDA;
   if (!mark(0)) return QMOE_ERR_CUDA;
   cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
                                n_tiles, err, ws + L.route_scratch, s);
@@ -304,6 +373,8 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p1.I = I;
   p1.swiglu_limit = swiglu_limit;
   p1.err = err;
+  p1.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
+  p1.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt1);
   e = launch_gemm(GemmKind::kFc1, rsched, map_x, p1, sms, s);
   if (e != cudaSuccess || !mark(3)) return QMOE_ERR_CUDA;
 
@@ -321,6 +392,8 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p2.topk_w = topk_weights_dev;
   p2.H = H;
   p2.err = err;
+  p2.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
+  p2.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt2);
   e = launch_gemm(GemmKind::kFc2, rsched, map_h, p2, sms, s);
   if (e != cudaSuccess || !mark(4)) return QMOE_ERR_CUDA;
 
@@ -377,18 +450,20 @@ int moe_nvfp4_forward_noalloc(const void* x_dev, const uint8_t* w13_fp4_dev,
   if (M == 0) return QMOE_OK;
   if (forward_layout(M, H, I, E, top_k, sched).total > (size_t)QMOE_NOALLOC_SCRATCH_BYTES)
     return QMOE_ERR_WORKSPACE;  // this batch needs more scratch than the built-in array
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMOE_ERR_CUDA;
-  if (!g_noalloc_addr[dev]) {
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
-      return QMOE_ERR_CUDA;
-    g_noalloc_addr[dev] = addr;
-  }
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != QMOE_OK) return rc;
   return forward_impl(x_dev, w13_fp4_dev, w13_scale_dev, w13_gscale_dev, w2_fp4_dev, w2_scale_dev,
                       w2_gscale_dev, topk_ids_dev, topk_weights_dev, out_dev, M, H, I, E, top_k,
-                      sched, g_noalloc_addr[dev], (size_t)QMOE_NOALLOC_SCRATCH_BYTES, stream,
-                      nullptr);
+                      sched, scratch, (size_t)QMOE_NOALLOC_SCRATCH_BYTES, stream, nullptr);
+}
+
+int qmoe_noalloc_read_error(void* stream, uint32_t* flags_out) {
+  if (!flags_out) return QMOE_ERR_ARG;
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != QMOE_OK) return rc;
+  return qmoe_read_error(scratch, stream, flags_out);
 }
 
 int moe_nvfp4_forward_events(const void* x_dev, const uint8_t* w13_fp4_dev,

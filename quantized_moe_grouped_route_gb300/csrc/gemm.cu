@@ -121,6 +121,83 @@ struct Cfg {
   static_assert((2 * RS + SL * (KS + 3) + 2 * ACCB + 1) * 8 + 16 <= 1024, "barrier area");
 };
 
+// Stream-K ranges of the decode schedule: CTA c of G takes the global steps
+// [sk_range_start(c), sk_range_start(c + 1)) of the n_steps steps of all units.
+__host__ __device__ __forceinline__ uint32_t sk_range_start(unsigned long long n_steps,
+                                                           unsigned int c, unsigned int G) {
+  return (uint32_t)(n_steps * c / G);
+}
+// Whether the decode schedule splits units between CTAs: only when dealing whole units
+// (ceil(n_units / G) per CTA at most) would leave more than 1/32 of the CTAs' unit slots
+// idle; otherwise the partial sums cost more than the balance gains.
+__host__ __device__ __forceinline__ bool sk_split(long long n_units, unsigned int G) {
+  const long long waves = (n_units + G - 1) / G;
+  return waves * (long long)G * 32 > n_units * 33;
+}
+// The CTA whose range holds global step g: the largest c with sk_range_start(c) <= g,
+// i.e. ceil((g + 1) G / n_steps) - 1.
+__host__ __device__ __forceinline__ unsigned int sk_cta_of(unsigned long long g,
+                                                          unsigned long long n_steps,
+                                                          unsigned int G) {
+  return (unsigned int)(((g + 1) * G + n_steps - 1) / n_steps - 1);
+}
+
+// Decode schedule, a unit split between CTAs: each segment's epilogue warp q stores its
+// 32 rows x 16 pairs of partial sums (fp32) in the CTA's slot (0 when the unit is the
+// CTA's first, else 1), then counts itself in the unit's arrival counter for quarter q.
+// The warp that arrives last sums all segments' partials in K order (CTA order), its own
+// from registers, the others' from global memory, into v and returns true; the others
+// return false.  The sum order does not depend on which segment arrives last, so the
+// result is deterministic; no warp waits for another.
+__device__ __forceinline__ bool sk_reduce(const GemmParams& p, float (&v)[16], int u, int nks,
+                                          unsigned long long n_steps, uint32_t g0, int lane,
+                                          int q) {
+  const unsigned int G = gridDim.x;
+  const int row = q * 32 + lane;
+  const int slot = (int)(g0 / (uint32_t)nks) == u ? 0 : 1;
+  float4* mine = reinterpret_cast<float4*>(p.sk_part + ((size_t)(blockIdx.x * 2 + slot) * 128 + row) * 16);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) mine[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  __threadfence();
+  __syncwarp();
+  const unsigned long long first = (unsigned long long)u * nks, last = first + nks - 1;
+  const unsigned int c0 = sk_cta_of(first, n_steps, G), c1 = sk_cta_of(last, n_steps, G);
+  int nseg = 0;
+  for (unsigned int c = c0; c <= c1; ++c)
+    nseg += sk_range_start(n_steps, c + 1, G) > sk_range_start(n_steps, c, G);
+  int old = 0;
+  if (lane == 0) old = atomicAdd(p.sk_cnt + (size_t)u * 4 + q, 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != nseg - 1) return false;
+  __threadfence();
+  float acc[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+  for (unsigned int c = c0; c <= c1; ++c) {
+    const uint32_t cs = sk_range_start(n_steps, c, G);
+    if (sk_range_start(n_steps, c + 1, G) == cs) continue;  // an empty range
+    if (c == blockIdx.x) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] += v[k];
+    } else {
+      const int sc = (int)(cs / (uint32_t)nks) == u ? 0 : 1;
+      const float4* src =
+          reinterpret_cast<const float4*>(p.sk_part + ((size_t)(c * 2 + sc) * 128 + row) * 16);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 w = __ldcg(src + k);
+        acc[4 * k] += w.x;
+        acc[4 * k + 1] += w.y;
+        acc[4 * k + 2] += w.z;
+        acc[4 * k + 3] += w.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c) v[c] = acc[c];
+  return true;
+}
+
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -203,9 +280,27 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   const int nks = (nb128 + KS - 1) / KS;  // pipeline steps per unit
   const int last_halves = nb128 - (nks - 1) * KS;
   const int n_units = (*p.n_tiles) * p.nrb;
-  // this CTA's units u = blockIdx.x, blockIdx.x + gridDim.x, .. of nks steps each
-  const int my_units = blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  const uint32_t total = (uint32_t)my_units * (uint32_t)nks;
+  // BIN (decode, stream-K): the units' K steps form one sequence of n_units * nks steps,
+  // cut into gridDim.x contiguous ranges, one per CTA; a unit split between CTAs is
+  // summed from their partial accumulators in K order (sk_reduce).  Otherwise each CTA
+  // takes whole units u = blockIdx.x, blockIdx.x + gridDim.x, ..
+  const unsigned long long n_steps = (unsigned long long)n_units * (unsigned long long)nks;
+  uint32_t g0 = 0, total = 0;
+  if constexpr (BIN) {
+    if (sk_split(n_units, gridDim.x)) {
+      g0 = sk_range_start(n_steps, blockIdx.x, gridDim.x);
+      total = sk_range_start(n_steps, blockIdx.x + 1, gridDim.x) - g0;
+    } else {  // whole units: a contiguous run of them per CTA, no partial sums
+      const uint32_t u0 = sk_range_start(n_units, blockIdx.x, gridDim.x);
+      const uint32_t u1 = sk_range_start(n_units, blockIdx.x + 1, gridDim.x);
+      g0 = u0 * (uint32_t)nks;
+      total = (u1 - u0) * (uint32_t)nks;
+    }
+  } else {
+    const int my_units =
+        blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    total = (uint32_t)my_units * (uint32_t)nks;
+  }
 
   if (warp == kWeightTmaWarp) {
     // ------------------------------------------------------------ weight TMA producer
@@ -214,26 +309,34 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     const uint64_t pol = l2_policy_evict_first();
     uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    // local step it: weights of step ks of unit u
+    auto issue = [&](int u, int ks) -> bool {
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t];
       const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nb128;
-      for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int s = it % RS;
-        if (!warp_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        const uint32_t nh = ks == nks - 1 ? (uint32_t)last_halves : (uint32_t)KS;
-        const size_t b0 = blk + (size_t)ks * KS;
-        const uint32_t st = smem_u32(rring + s * C::kStageBytes);
-        const uint32_t fb = smem_u32(&rfull[s]);
-        mbar_arrive_expect_tx_if(leader, fb, nh * kRawBytes);
-        bulk_g2s_if(leader, st, p.wcodes + b0 * kCodeBytes, nh * kCodeBytes, fb, pol);
-        bulk_g2s_if(leader, st + KS * kCodeBytes, p.wscales + b0 * kScaleBytes, nh * kScaleBytes,
-                    fb, pol);
+      const int s = it % RS;
+      if (!warp_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) return false;
+      const uint32_t nh = ks == nks - 1 ? (uint32_t)last_halves : (uint32_t)KS;
+      const size_t b0 = blk + (size_t)ks * KS;
+      const uint32_t st = smem_u32(rring + s * C::kStageBytes);
+      const uint32_t fb = smem_u32(&rfull[s]);
+      mbar_arrive_expect_tx_if(leader, fb, nh * kRawBytes);
+      bulk_g2s_if(leader, st, p.wcodes + b0 * kCodeBytes, nh * kCodeBytes, fb, pol);
+      bulk_g2s_if(leader, st + KS * kCodeBytes, p.wscales + b0 * kScaleBytes, nh * kScaleBytes,
+                  fb, pol);
+      return true;
+    };
+    if constexpr (BIN) {
+      for (; it < total && ok; ++it) {
+        const uint32_t g = g0 + it;
+        const int u = (int)(g / (uint32_t)nks);
+        ok = issue(u, (int)(g - (uint32_t)u * nks));
       }
+    } else {
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x)
+        for (int ks = 0; ks < nks && ok; ++ks, ++it) ok = issue(u, ks);
     }
+    if (!ok) --it;  // the failed step was not issued
     if (!ok) {  // let the copies already issued land before the CTA can exit
       const uint32_t first = it > (uint32_t)RS ? it - RS : 0u;
       for (uint32_t j = first; j < it; ++j) drain_wait(smem_u32(&rfull[j % RS]), (j / RS) & 1);
@@ -288,38 +391,42 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     const uint32_t bdesc_lo0 = (uint32_t)bdesc0, bdesc_hi = (uint32_t)(bdesc0 >> 32);
     uint32_t it = 0, local = 0;
     bool ok = true;
-    // BIN: the pair rows of global step g go into slot g % SL, whose previous step
-    // g - SL belongs to this warp too (SL % NMW == 0).  The copy for the warp's next
+    // BIN: the pair rows of local step i go into slot i % SL, whose previous step
+    // i - SL belongs to this warp too (SL % NMW == 0).  The copy for the warp's next
     // step is issued right after the MMAs of the current one, when the slot's previous
     // step (one own step back) has long completed: a step of lead for the copy.
-    uint32_t bg = (uint32_t)m, blu = 0, bks = (uint32_t)m;  // next copy: step, unit, K step
-    int bstart = 0;
+    uint32_t bg = (uint32_t)m;  // local step of the next copy
     const uint64_t bpol = l2_policy_evict_last();
     auto issue_b = [&]() -> bool {
       if (bg >= total) return true;
-      while (bks >= (uint32_t)nks) {
-        bks -= nks;
-        ++blu;
-      }
-      if (bks < (uint32_t)NMW || bg == (uint32_t)m) {  // entered a unit: its tile's first row
-        const int t = ((int)blockIdx.x + (int)blu * (int)gridDim.x) / p.nrb;
-        bstart = p.tiles[3 * t + 1];
-      }
+      const uint32_t g = g0 + bg;
+      const int u = (int)(g / (uint32_t)nks);
+      const int bks = (int)(g - (uint32_t)u * nks);
+      const int bstart = p.tiles[3 * (u / p.nrb) + 1];
       const uint32_t sl = bg % SL;
       if (!warp_wait(sempty_u + sl * 8, ((bg / SL) & 1) ^ 1, abort_flag, p.err)) return false;
       const uint32_t fb = sfull_u + sl * KS * 8;
       mbar_arrive_expect_tx_if(leader, fb, (uint32_t)C::kBBytes);
       tma_load_3d_if(leader, smem_u32(bring + sl * C::kBBytes), &tmap_b, 0, bstart,
-                     2 * KS * (int)bks, fb, bpol);
+                     2 * KS * bks, fb, bpol);
       bg += NMW;
-      bks += NMW;
       return true;
     };
     if constexpr (BIN) {
       grid_dep_wait();  // the pair rows are the previous kernel's output
       ok = issue_b();
     }
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++local) {
+    // BIN: segments (the part of one unit inside this CTA's step range) one after the
+    // other; otherwise whole units
+    int u = BIN ? 0 : (int)blockIdx.x;
+    while (ok && (BIN ? it < total : u < n_units)) {
+      int k0 = 0, len = nks;
+      if constexpr (BIN) {
+        const uint32_t g = g0 + it;
+        u = (int)(g / (uint32_t)nks);
+        k0 = (int)(g - (uint32_t)u * nks);
+        len = min(nks - k0, (int)(total - it));
+      }
       const int t = u / p.nrb;
       const int rows = p.tiles[3 * t + 2];
       const int n16 = ((rows + 15) >> 4) << 4;
@@ -333,9 +440,13 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem + C::kAccCol0 + (ab * NMW + m) * NMAX;
-      // this warp's first step of the unit: global step it + ks with (it + ks) % NMW == m
+      // this warp's first step of the segment: local step it + ks with (it + ks) % NMW == m
       const int ks0 = (m - (int)(it % NMW) + NMW) % NMW;
-      for (int ks = ks0; ks < nks; ks += NMW) {
+      // narrow prefill tiles: K slices dealt to several accumulator chains
+      int chains = 1, cstride = NMAX;
+      if constexpr (!BIN) acc_chains(n16, NMAX, chains, cstride);
+      uint32_t ch = 0, nsl = 0;
+      for (int ks = ks0; ks < len; ks += NMW) {
         const uint32_t sit = it + (uint32_t)ks;
         const int sl = sit % SL;
         const uint32_t sph = (sit / SL) & 1;
@@ -353,6 +464,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           if (NMAX > 256 && n16 > 256)
             mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0, b0, bdesc_hi, (256 * 128) >> 4,
                                 idesc, idesc2, acc);
+          else if (chains > 1)
+            mma_bf16_ts_slab4_chains(leader, d_tmem, cstride, chains, ch, nsl, a0, b0, bdesc_hi,
+                                     idesc);
           else
             mma_bf16_ts_slab4(leader, d_tmem, a0, b0, bdesc_hi, idesc, acc);
           tc_commit_if(leader, bempty0_u + sl * 8);
@@ -365,6 +479,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           if (NMAX > 256 && n16 > 256)
             mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0 + 32, b1, bdesc_hi,
                                 (256 * 128) >> 4, idesc, idesc2, 1u);
+          else if (chains > 1)
+            mma_bf16_ts_slab4_chains(leader, d_tmem, cstride, chains, ch, nsl, a0 + 32, b1,
+                                     bdesc_hi, idesc);
           else
             mma_bf16_ts_slab4(leader, d_tmem, a0 + 32, b1, bdesc_hi, idesc, 1u);
         } else {
@@ -372,7 +489,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
                             bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4, idesc,
                             ks != ks0 ? 1u : 0u);
         }
-        if (KS == 2 && (ks != nks - 1 || last_halves == 2)) {
+        if (KS == 2 && (k0 + ks != nks - 1 || last_halves == 2)) {
           if (!warp_wait(sfull_u + (sl * KS + 1) * 8, sph, abort_flag, p.err)) {
             ok = false;
             break;
@@ -390,7 +507,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           }
         }
       }
-      it += nks;
+      it += len;
+      ++local;
+      if constexpr (!BIN) u += gridDim.x;
       if (ok) tc_commit_if(leader, smem_u32(&accf[ab]));
     }
     // no MMA may still be running when TMEM is released
@@ -410,7 +529,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // DG, so the group meets the same ring residues on every lap (s, a) and the phase
     // bits flip on each wrap.
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
-    uint32_t pos = (uint32_t)grp % (uint32_t)nks;  // step of the current one within its unit
+    uint32_t pos = (g0 + (uint32_t)grp) % (uint32_t)nks;  // step of the current one within its unit
     for (uint32_t it = grp; it < total; it += DG) {
       const int nh = (KS == 2 && pos == (uint32_t)nks - 1) ? last_halves : KS;
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;
@@ -471,7 +590,15 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     constexpr int NCH = NMAX / 16;          // 16-column chunks of a tile
     constexpr int G = NMW == 1 ? 4 : 1;     // chunks per TMEM round trip
     uint32_t local = 0, it0 = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++local, it0 += nks) {
+    int u = BIN ? 0 : (int)blockIdx.x;
+    while (BIN ? it0 < total : u < n_units) {
+      int k0 = 0, len = nks;
+      if constexpr (BIN) {
+        const uint32_t g = g0 + it0;
+        u = (int)(g / (uint32_t)nks);
+        k0 = (int)(g - (uint32_t)u * nks);
+        len = min(nks - k0, (int)(total - it0));
+      }
       const int t = u / p.nrb, rb = u - t * p.nrb;
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
@@ -487,40 +614,76 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const uint32_t tbase =
           tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMW * NMAX;
       if constexpr (BIN) {
-        for (int c0 = 0; c0 < rows; c0 += 16) {
-          float v[16];
+        static_assert(!BIN || NMAX == 16, "the decode schedule's tiles are one 16-column chunk");
+        float v[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = 0.f;
-          // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this unit
-          // iff its first step ks0 = (m - it0 % NMW) mod NMW lies inside the unit
-          for (int m = 0; m < NMW; ++m) {
-            if ((m - (int)(it0 % NMW) + NMW) % NMW >= nks) continue;
-            uint32_t r[16];
-            tmem_ld_x16(tbase + m * NMAX + c0, r);
-            tmem_wait_ld();
-            tmem_ld_ready(r);
+        for (int c = 0; c < 16; ++c) v[c] = 0.f;
+        // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this segment
+        // iff its first step (m - it0 % NMW) mod NMW lies inside the segment
+        for (int m = 0; m < NMW; ++m) {
+          if ((m - (int)(it0 % NMW) + NMW) % NMW >= len) continue;
+          uint32_t r[16];
+          tmem_ld_x16(tbase + m * NMAX, r);
+          tmem_wait_ld();
+          tmem_ld_ready(r);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
-          }
-          epilogue_chunk_small<FC1, CLAMP>(p, v, lane, q, rb, start, rows, c0, gsc);
+          for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
         }
+        // the accumulator may be refilled once every warp has read it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&acce[ab]));
+        const bool whole = k0 == 0 && len == nks;
+        if (whole || sk_reduce(p, v, u, nks, n_steps, g0, lane, q))
+          epilogue_chunk_small<FC1, CLAMP>(p, v, lane, q, rb, start, rows, 0, gsc);
+        it0 += len;
+        ++local;
+        continue;
       } else {
         // warp m holds MMAs of this unit iff its first step ks0 = (m - it0 % NMW) mod NMW
         // lies inside the unit; accumulators are added in the fixed order m = 0, 1, ..
         bool has[NMW];
 #pragma unroll
         for (int m = 0; m < NMW; ++m) has[m] = (m - (int)(it0 % NMW) + NMW) % NMW < nks;
+        int chains = 1, cstride = NMAX;
+        acc_chains(((rows + 15) >> 4) << 4, NMAX, chains, cstride);
+        if (chains > 1) {
+        // a tile on several accumulator chains: each 16-column chunk is the sum of the
+        // chains in the fixed order 0, 1, ..
+#pragma unroll 1
+        for (int kc = 0; 16 * kc < rows; ++kc) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < chains; ++c) {
+            uint32_t r[16];
+            tmem_ld_x16(tbase + c * cstride + 16 * kc, r);
+            tmem_wait_ld();
+            tmem_ld_ready(r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
+          }
+          // (FC2: the chunk epilogue that broadcasts pair ids and weights by shuffles;
+          // the staged one would hold more registers than this kernel has)
+          if constexpr (FC1)
+            epilogue_chunk_fc1_tr<CLAMP>(p, v, lane, q, rb, start, rows, 16 * kc, gsc,
+                                         reinterpret_cast<uint8_t*>(st_pair));
+          else
+            epilogue_chunk_small<false>(p, v, lane, q, rb, start, rows, 16 * kc, gsc);
+        }
+        } else {
         // one batch body, reused (not unrolled: a smaller kernel, measurably faster)
 #pragma unroll 1
-        for (int k0 = 0; k0 < NCH; k0 += G) {
-          if (16 * k0 >= rows) break;
+        for (int kc = 0; kc < NCH; kc += G) {
+          if (16 * kc >= rows) break;
           uint32_t r[NMW][G][16];
 #pragma unroll
           for (int m = 0; m < NMW; ++m) {
             if (!has[m]) continue;
 #pragma unroll
             for (int g = 0; g < G; ++g)
-              if (16 * (k0 + g) < rows) tmem_ld_x16(tbase + m * NMAX + 16 * (k0 + g), r[m][g]);
+              if (16 * (kc + g) < rows) tmem_ld_x16(tbase + m * NMAX + 16 * (kc + g), r[m][g]);
           }
           tmem_wait_ld();
 #pragma unroll
@@ -528,11 +691,11 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
             if (!has[m]) continue;
 #pragma unroll
             for (int g = 0; g < G; ++g)
-              if (16 * (k0 + g) < rows) tmem_ld_ready(r[m][g]);
+              if (16 * (kc + g) < rows) tmem_ld_ready(r[m][g]);
           }
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            const int k = k0 + g;
+            const int k = kc + g;
             if (16 * k >= rows) break;
             float v[16];
 #pragma unroll
@@ -550,10 +713,14 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
               epilogue_chunk_fc2_staged(p, v, lane, q, rb, rows, 16 * k, st_pair, st_w);
           }
         }
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acce[ab]));
+      ++local;
+      it0 += nks;
+      u += gridDim.x;
     }
   }
 
@@ -617,9 +784,11 @@ cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, con
   // schedule then runs as the one-SM prefill one)
   const bool clamp = fc1 && std::isfinite(p.swiglu_limit);
   if (sched == QMOE_SCHED_DECODE) {
-    if (clamp) return run<16, 9, 3, 2, 3, 3, 2, true, true, true>(tmap_b, p, num_sms, stream);
-    return fc1 ? run<16, 9, 3, 2, 3, 3, 2, true, true>(tmap_b, p, num_sms, stream)
-               : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, num_sms, stream);
+    // stream-K: one CTA per SM, at most kMaxSkCtas (the partial buffer's slot pairs)
+    const int g = num_sms < kMaxSkCtas ? num_sms : kMaxSkCtas;
+    if (clamp) return run<16, 9, 3, 2, 3, 3, 2, true, true, true>(tmap_b, p, g, stream);
+    return fc1 ? run<16, 9, 3, 2, 3, 3, 2, true, true>(tmap_b, p, g, stream)
+               : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, g, stream);
   }
   if (sched == QMOE_SCHED_PREFILL_PAIR && !clamp && p.nrb % 2 == 0 && num_sms >= 2)
     return launch_gemm2(kind, tmap_b, p, num_sms, stream);

@@ -17,8 +17,9 @@ cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* 
                          unsigned int* err, void* scratch, cudaStream_t stream);
 
 // misc.cu
+// scale_layout: QMOE_SCALES_PLAIN, _SWIZZLED_128X4 or _PACKED_U32
 cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
-                          bool swizzled_scales, uint8_t* out_codes, uint8_t* out_scales,
+                          int scale_layout, uint8_t* out_codes, uint8_t* out_scales,
                           cudaStream_t stream);
 // pdl: launch with programmatic stream serialization (see pdl_attribute)
 cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
@@ -48,7 +49,18 @@ struct GemmParams {
   const float* topk_w;
   int H;
   unsigned int* err;
+  // decode schedule (stream-K): fp32 partial accumulators of units split between CTAs,
+  // [CTA][2 slots][128 rows][16 pairs], and one arrival counter per (unit, TMEM lane
+  // quarter), zero at launch
+  float* sk_part;
+  int* sk_cnt;
 };
+
+// Largest grid of the decode schedule (its partial buffer has a slot pair per CTA).
+constexpr int kMaxSkCtas = 192;
+// Bytes of the decode schedule's partial buffer and of its counters for one GEMM.
+inline size_t sk_part_bytes() { return (size_t)kMaxSkCtas * 2 * 128 * 16 * sizeof(float); }
+inline size_t sk_cnt_bytes(long long max_units) { return (size_t)max_units * 4 * sizeof(int); }
 
 // Launch attribute that lets a kernel start while the previous kernel on the stream
 // finishes (it must then call grid_dep_wait before reading that kernel's outputs).

@@ -36,13 +36,18 @@ __global__ void repack_codes_kernel(const uint8_t* __restrict__ w, int E, int N,
   }
 }
 
-// swz: the input scales are in the 128x4 swizzle of CUTLASS / FlashInfer NVFP4 weights
-// (megamoe_rm.cu page, scale_off): per expert, tiles of 128 rows x 4 scales, 512 bytes
-// each, the 4-column tile index fastest; inside a tile, row r's 4 scales at
-// (r % 32) * 16 + ((r / 32) % 4) * 4.  A row's 8 scales of one 128-wide K block are
-// then two 4-byte words, 512 bytes apart.
+// layout of the input scales (QMOE_SCALES_*):
+//  PLAIN          [E][N][K/16] bytes;
+//  SWIZZLED_128X4 the 128x4 swizzle of CUTLASS / FlashInfer NVFP4 weights (megamoe_rm.cu
+//                 page, scale_off): per expert, tiles of 128 rows x 4 scales, 512 bytes
+//                 each, the 4-column tile index fastest; inside a tile, row r's 4
+//                 scales at (r % 32) * 16 + ((r / 32) % 4) * 4.  A row's 8 scales of one
+//                 128-wide K block are then two 4-byte words, 512 bytes apart;
+//  PACKED_U32     [E][N][K/64] uint32 words (tilelang_kernels.py page,
+//                 grouped_gemm_fp4_packed_sf), scale j of word g (K block 4g + j) in
+//                 bits 8j..8j+7: a 128-wide K block's 8 scales are words 2ks, 2ks + 1.
 __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N, int K, int w13,
-                                     int swz, uint2* __restrict__ out) {
+                                     int layout, uint2* __restrict__ out) {
   const int nrb = N / 128, nks = K / 128;
   const long long total = (long long)E * N * nks;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -55,7 +60,19 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N
     const int e = (int)(rest / nrb);
     const int n = repack_row(w13 != 0, N, rb, r);
     const size_t C = (size_t)(K / 16);
-    if (swz) {
+    if (layout == QMOE_SCALES_PACKED_U32) {
+      const uint32_t* wrow = reinterpret_cast<const uint32_t*>(s) + ((size_t)e * N + n) * (C / 4);
+      // output byte b of the step = scale of K block 8 ks + b (bits 8b.. of the words)
+      uint32_t o[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t wv = wrow[2 * ks + h];
+        o[h] = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[h] |= ((wv >> (8 * j)) & 0xFFu) << (8 * j);
+      }
+      out[idx] = make_uint2(o[0], o[1]);
+    } else if (layout == QMOE_SCALES_SWIZZLED_128X4) {
       const uint8_t* se = s + (size_t)e * N * C;
       const size_t o = ((size_t)(n >> 7) * (C >> 2) + (size_t)ks * 2) * 512 + (size_t)(n & 31) * 16 +
                        (size_t)((n >> 5) & 3) * 4;
@@ -179,7 +196,7 @@ int grid_for(long long work, int threads, int num_sms) {
 }  // namespace
 
 cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int K, bool w13,
-                          bool swizzled_scales, uint8_t* out_codes, uint8_t* out_scales,
+                          int scale_layout, uint8_t* out_codes, uint8_t* out_scales,
                           cudaStream_t stream) {
   const long long words = (long long)E * N * (K / 8);
   const long long rows = (long long)E * N * (K / 128);
@@ -188,7 +205,7 @@ cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int 
   cudaError_t rc = cudaGetLastError();
   if (rc != cudaSuccess) return rc;
   repack_scales_kernel<<<grid_for(rows, 256, 1184), 256, 0, stream>>>(
-      s, E, N, K, w13 ? 1 : 0, swizzled_scales ? 1 : 0, reinterpret_cast<uint2*>(out_scales));
+      s, E, N, K, w13 ? 1 : 0, scale_layout, reinterpret_cast<uint2*>(out_scales));
   return cudaGetLastError();
 }
 

@@ -36,6 +36,7 @@ QMOE_W13 = 1
 QMOE_W2 = 2
 QMOE_SCALES_PLAIN = 0
 QMOE_SCALES_SWIZZLED_128X4 = 1
+QMOE_SCALES_PACKED_U32 = 2
 
 _ERRORS = {QMOE_ERR_ARG: "argument", QMOE_ERR_SHAPE: "shape", QMOE_ERR_CUDA: "cuda",
            QMOE_ERR_TIMEOUT: "timeout", QMOE_ERR_ARCH: "arch", QMOE_ERR_WORKSPACE: "workspace",
@@ -86,6 +87,7 @@ def _bind(L):
         "qmoe_forward_workspace_layout": (i32, [i32, i32, i32, i32, i32, i32,
                                                 ctypes.POINTER(ctypes.c_size_t)]),
         "qmoe_read_error": (i32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
+        "qmoe_noalloc_read_error": (i32, [P, ctypes.POINTER(ctypes.c_uint32)]),
         "qmoe_selftest_dequant": (i32, [P, P]),
         "qmoe_selftest_timeout": (i32, [P, i64, P]),
     }
@@ -211,13 +213,20 @@ def moe_route(topk_ids: torch.Tensor, E: int, tile_n: int, stream=None):
 def moe_nvfp4_repack(w_fp4: torch.Tensor, w_scale: torch.Tensor, which: int, stream=None,
                      scale_layout: int = QMOE_SCALES_PLAIN):
     """Plain [E][N][K/2] codes + block scales -> repacked (codes, scales).  Scales are
-    [E][N][K/16] (QMOE_SCALES_PLAIN) or, with QMOE_SCALES_SWIZZLED_128X4, N*K/16 bytes
-    per expert in the 128x4 swizzle of CUTLASS / FlashInfer checkpoints."""
+    [E][N][K/16] bytes (QMOE_SCALES_PLAIN), N*K/16 bytes per expert in the 128x4
+    swizzle of CUTLASS / FlashInfer checkpoints (QMOE_SCALES_SWIZZLED_128X4), or
+    [E][N][K/64] int32 words of four scales each (QMOE_SCALES_PACKED_U32)."""
     _need(w_fp4, torch.uint8, "w_fp4")
-    _need(w_scale, torch.uint8, "w_scale")
     E, N, K2 = w_fp4.shape
     K = 2 * K2
-    if w_scale.numel() != E * N * (K // 16) or w_scale.shape[0] != E:
+    if scale_layout == QMOE_SCALES_PACKED_U32:
+        _need(w_scale, torch.int32, "w_scale")
+        if tuple(w_scale.shape) != (E, N, K // 64):
+            raise ValueError("packed w_scale must be int32 [E][N][K/64]")
+    else:
+        _need(w_scale, torch.uint8, "w_scale")
+    nbytes = w_scale.numel() * w_scale.element_size()
+    if nbytes != E * N * (K // 16) or w_scale.shape[0] != E:
         raise ValueError("w_scale shape does not match w_fp4")
     if scale_layout == QMOE_SCALES_PLAIN and tuple(w_scale.shape) != (E, N, K // 16):
         raise ValueError("plain w_scale must be [E][N][K/16]")
@@ -308,6 +317,14 @@ def qmoe_read_error(workspace: torch.Tensor, stream=None):
     """(return code, flags) of the device error word at the start of a workspace."""
     flags = ctypes.c_uint32(0)
     rc = lib().qmoe_read_error(_ptr(workspace), _stream(stream), ctypes.byref(flags))
+    return rc, flags.value
+
+
+def qmoe_noalloc_read_error(stream=None):
+    """(return code, flags) of the error word of the library's built-in scratch array
+    (the last moe_nvfp4_forward_noalloc call on the current device)."""
+    flags = ctypes.c_uint32(0)
+    rc = lib().qmoe_noalloc_read_error(_stream(stream), ctypes.byref(flags))
     return rc, flags.value
 
 
