@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true",
                     help="skip the untimed clock-sampling soak (for profiler launch lists)")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time only the headline workload (not the other decode / prefill ones)")
     return ap.parse_args()
 
 
@@ -144,10 +146,12 @@ class ClockSampler:
         if self.thread:
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for _, line in self.lines:
+        for t, line in list(self.lines):
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -230,32 +234,56 @@ def reference_arm(args, rank, world):
     return 0
 
 
-def ours_arm(args, rank, world, local):
+# Workloads timed in the same run besides the headline one (one line, "configs" key):
+# the other decode shape and both prefill shapes of the pages' workloads.
+EXTRA_CONFIGS = ["decode_m1_h7168_i3072_e32_k8", "prefill_zipf_m2048_h4096_i1536_e128_k8",
+                 "prefill_m8192_h7168_i2048_e256_k8"]
+
+
+def is_decode(qmoe, sched, M, top_k, E):
+    return sched == qmoe.QMOE_SCHED_DECODE or (sched == qmoe.QMOE_SCHED_AUTO and M * top_k <= 4 * E)
+
+
+def roofline_entry(cfg, alg, stage_ms, decode, sched_name, peaks):
+    """Roofline of the dominant kernel (FC1): HBM bytes on decode, tensor FLOPs on prefill."""
+    hbm_gbs, bf16_tf, _, peak_kind = peaks
+    if decode:
+        ach = alg["fc1"] / (stage_ms["fc1"] * 1e-3) / 1e9
+        return {"kernel": f"moe_gemm_kernel<FC1,{sched_name}>", "bound": "hbm", "achieved": ach,
+                "peak": hbm_gbs, "unit": "GB/s", "frac": ach / hbm_gbs,
+                "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
+                "algorithmic_bytes_per_launch": alg["fc1"],
+                "traffic": measured_traffic("fc1", cfg.name)}
+    fl = 2.0 * alg["pairs"] * 2 * cfg.H * cfg.I
+    ach = fl / (stage_ms["fc1"] * 1e-3) / 1e12
+    return {"kernel": f"moe_gemm_kernel<FC1,{sched_name}>", "bound": "tensor", "achieved": ach,
+            "peak": bf16_tf, "unit": "TFLOP/s", "frac": ach / bf16_tf,
+            "peak_kind": f"{peak_kind} (bf16_tflops, burst)", "algorithmic_flops_per_launch": fl,
+            "traffic": measured_traffic("fc1", cfg.name)}
+
+
+def time_workload(cfg, sched, K, warmup, dev, rank, world, barrier, token_seed=None,
+                  keep_plain=False):
+    """Build one workload, warm up, time K forwards (one region, CUDA events on the
+    launching stream), then K more with the library's stage events for per-kernel times.
+    Returns everything the JSON line reports about it, plus the objects e2e needs."""
     import torch
-    import torch.distributed as dist
 
     from quantized_moe_grouped_route_gb300 import NVFP4MoE, qmoe
-    from qmoe_inputs.gen import config_by_name, make_inputs
+    from qmoe_inputs.gen import make_inputs
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-    cfg = config_by_name(args.config)
-    sched = {"auto": qmoe.QMOE_SCHED_AUTO, "decode": qmoe.QMOE_SCHED_DECODE,
-             "prefill": qmoe.QMOE_SCHED_PREFILL,
-             "prefill_pair": qmoe.QMOE_SCHED_PREFILL_PAIR}[args.sched]
-    li = make_inputs(cfg, dev, token_seed=cfg.seed + 1000 * rank)
+    li = make_inputs(cfg, dev, token_seed=token_seed)
     torch.cuda.synchronize()
-
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     r0.record()
     layer = NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
     r1.record()
     torch.cuda.synchronize()
     repack_ms = r0.elapsed_time(r1)
-
     M, H, I, E, top_k = cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k
+    if not keep_plain:  # only the repacked weights are read from here on
+        li.w13 = li.s13 = li.w2 = li.s2 = None
+        torch.cuda.empty_cache()
     ws = layer.workspace(M, top_k, sched, dev)
     out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
@@ -271,51 +299,90 @@ def ours_arm(args, rank, world, local):
                                           events, H=H, I=I, E=E, sched=sched, workspace=ws,
                                           stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     rc, flags = qmoe.qmoe_read_error(ws)
     if rc != 0:
-        raise RuntimeError(f"device error word after warm-up: rc={rc} flags={flags}")
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    t_soak = time.time()
-    while not args.no_soak and time.time() - t_soak < 0.6:  # let the sampler see the GPU under this load
-        for _ in range(20):
-            step()
-        torch.cuda.synchronize()
-
-    K = args.steps
+        raise RuntimeError(f"{cfg.name}: device error word after warm-up: rc={rc} flags={flags}")
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     for row in evs:  # torch creates the CUDA event on first record
         for ev in row:
             ev.record()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
+    barrier()
     torch.cuda.synchronize()
+    wall0 = time.time()
     t0.record()
-    for i in range(K):
+    for _ in range(K):
         step()
     t1.record()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    sampler.stop()
+    wall1 = time.time()
+    barrier()
     ms = t0.elapsed_time(t1) / K
-    # per-kernel durations: the same K steps again with the library's stage events
-    # (an event between two kernels keeps the later one from starting early, so these
-    # are each kernel's own durations)
+    # per-kernel durations: the same K steps again with the library's stage events (an
+    # event between two kernels keeps the later one from starting early, so these are
+    # each kernel's own durations); the median of the K steps is reported as well
     for i in range(K):
         step(evs[i])
     torch.cuda.synchronize()
     stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                 for j, s in enumerate(STAGES)}
-    ms = max_over_ranks(ms, world, dev)
+    step_median = statistics.median(evs[i][0].elapsed_time(evs[i][5]) for i in range(K))
+    rc, flags = qmoe.qmoe_read_error(ws)
+    if rc != 0:
+        raise RuntimeError(f"{cfg.name}: device error word after the timed region: rc={rc} "
+                           f"flags={flags}")
+    return {"li": li, "layer": layer, "ws": ws, "out": out, "stream": stream, "ms": ms,
+            "stage_ms": stage_ms, "step_median_ms": step_median, "repack_ms": repack_ms,
+            "window": (wall0, wall1)}
+
+
+def ours_arm(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_moe_grouped_route_gb300 import qmoe
+    from qmoe_inputs.gen import config_by_name
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    cfg = config_by_name(args.config)
+    sched = {"auto": qmoe.QMOE_SCHED_AUTO, "decode": qmoe.QMOE_SCHED_DECODE,
+             "prefill": qmoe.QMOE_SCHED_PREFILL,
+             "prefill_pair": qmoe.QMOE_SCHED_PREFILL_PAIR}[args.sched]
+    M, H, I, E, top_k = cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if not args.no_soak:  # let the sampler see the GPU under this load before the timed region
+        w = time_workload(cfg, sched, 20, args.warmup, dev, rank, world, barrier,
+                          token_seed=cfg.seed + 1000 * rank)
+        t_soak = time.time()
+        while time.time() - t_soak < 0.6:
+            for _ in range(20):
+                qmoe.moe_nvfp4_forward(w["li"].x, w["layer"].w13c, w["layer"].w13s,
+                                       w["layer"].gs13, w["layer"].w2c, w["layer"].w2s,
+                                       w["layer"].gs2, w["li"].topk_ids, w["li"].topk_weights,
+                                       w["out"], H=H, I=I, E=E, sched=sched, workspace=w["ws"])
+            torch.cuda.synchronize()
+        del w
+    main = time_workload(cfg, sched, args.steps, args.warmup, dev, rank, world, barrier,
+                         token_seed=cfg.seed + 1000 * rank, keep_plain=True)
+    ms = max_over_ranks(main["ms"], world, dev)
+    li, layer, out, stream = main["li"], main["layer"], main["out"], main["stream"]
 
     # end to end through the public call with host buffers: H2D of the step's inputs
     # from pinned memory, the layer, D2H of the result, all inside the timed region
+    K = args.steps
     hx = li.x.cpu().pin_memory()
     hids = li.topk_ids.cpu().pin_memory()
     hw = li.topk_weights.cpu().pin_memory()
@@ -334,8 +401,7 @@ def ours_arm(args, rank, world, local):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
+    barrier()
     e0.record()
     for _ in range(K):
         e2e_step()
@@ -345,37 +411,53 @@ def ours_arm(args, rank, world, local):
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
     d2h = hout.numel() * 2
-
-    rc, flags = qmoe.qmoe_read_error(ws)
+    rc, flags = qmoe.qmoe_read_error(main["ws"])
     if rc != 0:
-        raise RuntimeError(f"device error word after the timed region: rc={rc} flags={flags}")
+        raise RuntimeError(f"device error word after the e2e leg: rc={rc} flags={flags}")
+
+    peaks = load_peaks()
+    hbm_gbs = peaks[0]
+    alg = algorithmic_bytes(cfg, li.topk_ids.cpu())
+    decode = is_decode(qmoe, sched, M, top_k, E)
+    sched_name = "decode" if decode else "prefill"
+    roof = roofline_entry(cfg, alg, main["stage_ms"], decode, sched_name, peaks)
+
+    # the other workloads of the pages, timed in the same run (rank 0's line reports them;
+    # every rank runs them so that the barriers match)
+    extra = {}
+    if world == 1 and not args.no_extra_configs and args.config == DEFAULT_CONFIG:
+        steps_x = max(20, min(K, 50))
+        for name in EXTRA_CONFIGS:
+            c = config_by_name(name)
+            r = time_workload(c, qmoe.QMOE_SCHED_AUTO, steps_x, args.warmup, dev, rank, world,
+                              barrier)
+            a = algorithmic_bytes(c, r["li"].topk_ids.cpu())
+            dec = is_decode(qmoe, qmoe.QMOE_SCHED_AUTO, c.M, c.top_k, c.E)
+            sn = "decode" if dec else "prefill"
+            rf = roofline_entry(c, a, r["stage_ms"], dec, sn, peaks)
+            layer_frac = (a["weights"] / (r["ms"] * 1e-3) / 1e9 / hbm_gbs if dec else
+                          a["flops"] / (r["ms"] * 1e-3) / 1e12 / peaks[1])
+            extra[name] = {
+                "M": c.M, "H": c.H, "I": c.I, "E": c.E, "top_k": c.top_k, "sched": sn,
+                "steps": steps_x, "ms_per_step": r["ms"], "step_median_ms": r["step_median_ms"],
+                "tokens_per_s": c.M / (r["ms"] * 1e-3), "stages_ms": r["stage_ms"],
+                "roofline": rf,
+                "layer": {"bound": "hbm" if dec else "tensor", "frac": layer_frac,
+                          "weight_gbs": a["weights"] / (r["ms"] * 1e-3) / 1e9,
+                          "tflops": a["flops"] / (r["ms"] * 1e-3) / 1e12},
+                "touched_experts": a["touched_experts"],
+                "clocks": sampler.summary(*r["window"]),
+                "l2": ("inputs larger than L2: "
+                       f"{a['weights'] / 1e9:.2f} GB of touched expert weights per step"),
+            }
+            del r
+            torch.cuda.empty_cache()
+    sampler.stop()
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
-
-    hbm_gbs, bf16_tf, bf16_tf_sus, peak_kind = load_peaks()
-    alg = algorithmic_bytes(cfg, li.topk_ids.cpu())
-    decode = (sched == qmoe.QMOE_SCHED_DECODE or
-              (sched == qmoe.QMOE_SCHED_AUTO and M * top_k <= 4 * E))
-    sched_name = "decode" if decode else "prefill"
-    if decode:
-        dom = "fc1"
-        ach = alg["fc1"] / (stage_ms["fc1"] * 1e-3) / 1e9
-        roof = {"kernel": f"moe_gemm_kernel<FC1,{sched_name}>", "bound": "hbm",
-                "achieved": ach, "peak": hbm_gbs, "unit": "GB/s", "frac": ach / hbm_gbs,
-                "peak_kind": f"{peak_kind} (hbm_gbs, burst)",
-                "algorithmic_bytes_per_launch": alg["fc1"],
-                "traffic": measured_traffic("fc1", cfg.name)}
-    else:
-        dom = "fc1"
-        fl = 2.0 * alg["pairs"] * 2 * H * I
-        ach = fl / (stage_ms["fc1"] * 1e-3) / 1e12
-        roof = {"kernel": f"moe_gemm_kernel<FC1,{sched_name}>", "bound": "tensor",
-                "achieved": ach, "peak": bf16_tf, "unit": "TFLOP/s", "frac": ach / bf16_tf,
-                "peak_kind": f"{peak_kind} (bf16_tflops, burst)",
-                "algorithmic_flops_per_launch": fl,
-                "traffic": measured_traffic("fc1", cfg.name)}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -400,14 +482,16 @@ def ours_arm(args, rank, world, local):
         "gpu_launches": qmoe.qmoe_forward_kernel_count(M, top_k, E, sched) * K,
         "roofline": roof,
         "cpu_baseline": cpu,
-        "clocks": sampler.summary(),
-        "stages_ms": stage_ms,
+        "clocks": sampler.summary(*main["window"]),
+        "stages_ms": main["stage_ms"],
         "stages_from": "a second pass of the same steps with stage events (kernels serialised)",
+        "step_median_ms": main["step_median_ms"],
         "weight_gbs": alg["weights"] / (ms * 1e-3) / 1e9,
         "hbm_frac_layer": alg["weights"] / (ms * 1e-3) / 1e9 / hbm_gbs,
         "tflops": alg["flops"] / (ms * 1e-3) / 1e12,
         "touched_experts": alg["touched_experts"],
-        "repack_ms": repack_ms,
+        "repack_ms": main["repack_ms"],
+        "configs": extra or None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

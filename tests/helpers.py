@@ -14,10 +14,11 @@ RMS_TOL = 2e-3
 # Largest share of h values whose bf16 rounding may differ from the oracle's own.  A
 # flip is legitimate only when the exact SiLU(gate)*up lies within the GPU's fp32
 # accumulation noise of a bf16 rounding midpoint.  The limit comes from an emulation of
-# that accumulation at H = 7168 (tests/test_h_rounding_bound.py): with truncating fp32
-# additions, the least favourable arithmetic a tensor core could use, the emulated rate
-# stays below 2e-3 (round-to-nearest: below 5e-4); the limit is that bound.
-MAX_FLIP_RATE = 2e-3
+# that accumulation at H = 7168 (tests/test_h_rounding_bound.py): 3.4e-4 of the values
+# flip with round-to-nearest additions, 1.4e-3 with truncating ones (the least
+# favourable rounding, and the one the GPU's measured rates match: 1.6e-3 on the large
+# prefill workload); the limit is about twice the truncating rate.
+MAX_FLIP_RATE = 3e-3
 
 # Largest share of compared output elements allowed outside the tolerance against the
 # unconditioned oracle; each of them must also be explained by a validated h flip in

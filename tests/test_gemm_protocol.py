@@ -48,13 +48,29 @@ def check(cond, msg):
         raise ProtocolError(msg)
 
 
-def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None):
-    """One CTA running n_units units of nb128 weight blocks each.  Returns normally or
-    raises ProtocolError (unsafe access) / RuntimeError (deadlock)."""
+def segments(g0, total, nks):
+    """Stream-K (BIN): the (unit, first step, steps) pieces of the global steps
+    [g0, g0 + total), as the kernel's MMA and epilogue loops cut them."""
+    out, it = [], 0
+    while it < total:
+        g = g0 + it
+        u, k0 = divmod(g, nks)
+        n = min(nks - k0, total - it)
+        out.append((u, k0, n))
+        it += n
+    return out
+
+
+def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None, g0=0):
+    """One CTA running n_units units of nb128 weight blocks each (BIN: the global steps
+    [g0, g0 + n_units * nks) of the stream-K sequence, which may start and end inside
+    a unit).  Returns normally or raises ProtocolError (unsafe access) / RuntimeError
+    (deadlock)."""
     rng = random.Random(seed)
     nks = -(-nb128 // KS)
     last_halves = nb128 - (nks - 1) * KS
     total = n_units * nks
+    segs = segments(g0, total, nks) if BIN else [(u, 0, nks) for u in range(n_units)]
     rfull = [Bar(1) for _ in range(RS)]
     rempty = [Bar(4) for _ in range(RS)]
     sfull = [Bar(5 if h == 0 else 4) for _ in range(SL) for h in range(KS)]
@@ -78,7 +94,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
     drained_by = [[-1] * 4 for _ in range(ACCB)]
 
     def step_blocks(it):
-        return last_halves if (it % nks) == nks - 1 else KS
+        return last_halves if ((g0 + it) % nks) == nks - 1 else KS
 
     def weight_producer():
         for it in range(total):
@@ -137,14 +153,14 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
         if BIN:
             yield from issue_b()
         it = 0
-        for local in range(n_units):
+        for local, (_, k0, seg_len) in enumerate(segs):
             ab = local % ACCB
             while not acce[ab].done(((local // ACCB) & 1) ^ 1):
                 yield False
             check(local < ACCB or drained[ab] >= local - ACCB,
                   f"accumulator {ab} written for unit {local} before unit {local - ACCB} was drained")
             ks0 = (m - it % NMW + NMW) % NMW
-            for ks in range(ks0, nks, NMW):
+            for ks in range(ks0, seg_len, NMW):
                 sit = it + ks
                 sl, sph = sit % SL, (sit // SL) & 1
                 while not sfull[sl * KS].done(sph):
@@ -159,7 +175,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
                         while not bfull1[sl].done(sph):
                             yield False
                     check(b_slab[sl][1] == sit, f"slab {sl}.1 not landed for step {sit}")
-                if KS == 2 and (ks != nks - 1 or last_halves == 2):
+                if KS == 2 and (k0 + ks != nks - 1 or last_halves == 2):
                     while not sfull[sl * KS + 1].done(sph):
                         yield False
                     check(all(v == sit for v in a_slot[sl][1]),
@@ -172,7 +188,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
                 if BIN:
                     yield from issue_b()
                 yield True
-            it += nks
+            it += seg_len
 
             def unit_done(ab=ab, local=local):
                 unit_mma_done[ab][m] = local
@@ -198,7 +214,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
             yield True
 
     def epilogue_warp(q):
-        for local in range(n_units):
+        for local in range(len(segs)):
             ab = local % ACCB
             while not accf[ab].done((local // ACCB) & 1):
                 yield False
@@ -251,6 +267,89 @@ PREFILL_NARROW = dict(NMW=1, SL=2, RS=8, DG=2, ACCB=2, KS=1, BIN=False)
 def test_protocol_is_safe_and_live(cfg, nb128):
     for seed in range(12):
         simulate(**cfg, nb128=nb128, n_units=5, seed=seed)
+
+
+@pytest.mark.parametrize("nb128,g0", [(7, 5), (16, 3), (16, 15), (3, 1), (2, 0)])
+def test_stream_k_ranges_are_safe_and_live(nb128, g0):
+    """The decode schedule's CTAs start and end inside units (stream-K)."""
+    for seed in range(12):
+        simulate(**DECODE, nb128=nb128, n_units=4, seed=seed, g0=g0)
+
+
+def _range_start(n_steps, c, G):
+    return n_steps * c // G
+
+
+def _cta_of(g, n_steps, G):
+    return ((g + 1) * G + n_steps - 1) // n_steps - 1
+
+
+def _split(n_units, G):
+    waves = (n_units + G - 1) // G
+    return waves * G * 32 > n_units * 33
+
+
+def test_stream_k_split_rule():
+    """Units are split between CTAs only where whole units would idle more than 1/32 of
+    the last wave: the decode workloads' FC1 (384 and 3200 units on 152 CTAs) split,
+    their FC2 (448 and 5600 units) do not."""
+    assert _split(384, 152) and _split(3200, 152)
+    assert not _split(448, 152) and not _split(5600, 152)
+    assert not _split(152, 152) and _split(153, 152) and _split(1, 152)
+
+
+@pytest.mark.parametrize("n_units,G", [(448, 152), (5600, 152), (7, 3), (1, 1)])
+def test_whole_unit_ranges(n_units, G):
+    """Without splitting, CTA c takes units [n_units c / G, n_units (c + 1) / G): every unit
+    once, at most ceil(n_units / G) per CTA, no partial pieces."""
+    nks = 5
+    seen = []
+    for c in range(G):
+        u0, u1 = _range_start(n_units, c, G), _range_start(n_units, c + 1, G)
+        assert u1 - u0 <= -(-n_units // G)
+        for u, k0, n in segments(u0 * nks, (u1 - u0) * nks, nks):
+            assert k0 == 0 and n == nks
+            seen.append(u)
+    assert seen == list(range(n_units))
+
+
+@pytest.mark.parametrize("n_units,nks,G", [(384, 28, 152), (3200, 28, 152), (448, 12, 152),
+                                           (1, 28, 152), (3, 4, 152), (5, 1, 7), (152, 1, 152),
+                                           (153, 2, 152), (7, 28, 10), (1, 1, 1)])
+def test_stream_k_partition_and_reduction(n_units, nks, G):
+    """The formulas of the decode schedule's stream-K split (sk_range_start, sk_cta_of and
+    the partial slots of sk_reduce in csrc/gemm.cu), over all CTAs: every step is in
+    exactly one range; a unit's pieces lie in the CTAs sk_cta_of names, in K order; the
+    pieces counted by the reduction are the real ones; no CTA writes two partials into
+    one slot, and the reducer reads each CTA's partial from the slot it was written to."""
+    T = n_units * nks
+    starts = [_range_start(T, c, G) for c in range(G + 1)]
+    assert starts[0] == 0 and starts[G] == T
+    owner = {}
+    written = {}  # (cta, slot) -> unit
+    pieces = {u: [] for u in range(n_units)}
+    for c in range(G):
+        g0, total = starts[c], starts[c + 1] - starts[c]
+        for u, k0, n in segments(g0, total, nks):
+            for k in range(k0, k0 + n):
+                assert (u, k) not in owner
+                owner[(u, k)] = c
+            pieces[u].append((c, k0, n))
+            if not (k0 == 0 and n == nks):          # a partial: sk_reduce stores it
+                slot = 0 if g0 // nks == u else 1
+                assert (c, slot) not in written, "two partials in one slot"
+                written[(c, slot)] = u
+    assert len(owner) == T
+    for u, ps in pieces.items():
+        c0, c1 = _cta_of(u * nks, T, G), _cta_of(u * nks + nks - 1, T, G)
+        real = [c for c, _, _ in ps]
+        counted = [c for c in range(c0, c1 + 1) if starts[c + 1] > starts[c]]
+        assert counted == real == sorted(real)
+        assert [k0 for _, k0, _ in ps] == sorted(k0 for _, k0, _ in ps)
+        if len(ps) > 1:
+            for c in real:
+                slot = 0 if starts[c] // nks == u else 1
+                assert written[(c, slot)] == u
 
 
 @pytest.mark.parametrize("plant,cfg", [("slab1_on_bempty0", PREFILL_WIDE),

@@ -3,7 +3,6 @@ CPU oracle: small shapes element by element, the five workload configs at full
 size on sampled tokens (the benchmark's launch configuration), edge cases and
 determinism.  Tolerance per element: |got - ref| <= 2e-2 |ref| + 2e-3 rms(ref)."""
 
-import numpy as np
 import pytest
 import torch
 
@@ -33,6 +32,10 @@ SMALL = [
     # experts of 257..320 pairs (one two-chain prefill tile) and of more (a tail tile)
     ("m580_h256_i128_e2_k1", 580, 256, 128, 2, 1),
     ("m700_h256_i256_e2_k1", 700, 256, 256, 2, 1),
+    # decode schedule, stream-K: fewer K steps than CTAs (units split over up to four
+    # CTAs, most CTAs idle) and a few steps per CTA (units split over many CTAs)
+    ("sk_m1_h1024_i1024_e4_k1", 1, 1024, 1024, 4, 1),
+    ("sk_m3_h7168_i512_e2_k2", 3, 7168, 512, 2, 2),
 ]
 
 
@@ -93,15 +96,17 @@ def test_zero_tokens_is_a_noop():
 
 @pytest.mark.parametrize("cfg", [c for c in CONFIGS if c.name.startswith("prefill")],
                          ids=lambda c: c.name)
-def test_prefill_pair_schedule_is_bit_identical(cfg):
-    """The two-SM prefill GEMM accumulates each output in the same K order as the
-    one-SM kernel (whose results the oracle checks above), so the two schedules must
-    agree bit for bit on the full workloads; each is also run-to-run deterministic."""
+def test_prefill_pair_schedule_full_size(cfg):
+    """The two-SM prefill GEMM on the full prefill workloads: run-to-run deterministic and
+    within the tolerance of the oracle on the forced tokens.  (It accumulates each
+    output on one chain in K order; the one-SM kernel splits narrow tiles over several
+    chains, so the two agree to rounding, not bit for bit.)"""
     li = make_inputs(cfg, "cuda")
     layer = qmoe.NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
-    outs = [layer(li.x, li.topk_ids, li.topk_weights, sched=s).view(torch.int16).clone()
-            for s in (qmoe.QMOE_SCHED_PREFILL, qmoe.QMOE_SCHED_PREFILL_PAIR,
-                      qmoe.QMOE_SCHED_PREFILL_PAIR)]
+    s = qmoe.QMOE_SCHED_PREFILL_PAIR
+    outs = [layer(li.x, li.topk_ids, li.topk_weights, sched=s).clone() for _ in range(2)]
     torch.cuda.synchronize()
-    assert torch.equal(outs[1], outs[2]), "two-SM schedule not deterministic"
-    assert torch.equal(outs[0], outs[1]), "two-SM and one-SM schedules differ"
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), \
+        "two-SM schedule not deterministic"
+    toks = forced_tokens(li, s, n_random=32, seed=cfg.seed)
+    check_layer(li, outs[1], layer._ws, s, tokens=toks, what=f"{cfg.name} two-SM")

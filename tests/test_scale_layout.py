@@ -48,3 +48,22 @@ def test_bad_shapes_rejected():
         scale_layout.swizzled_offsets(100, 8)
     with pytest.raises(ValueError):
         scale_layout.swizzled_offsets(128, 6)
+
+
+def test_packed_u32_word_holds_four_consecutive_blocks():
+    """uint32-packed scales (tilelang_kernels.py page, grouped_gemm_fp4_packed_sf), read
+    as: scale of K block 4g + j in bits 8j..8j+7 of word g."""
+    plain = np.array([[[0x38, 0x40, 0x01, 0x7E, 0x00, 0x08, 0x30, 0x48]]], np.uint8)
+    words = scale_layout.pack_u32(plain)
+    assert words.shape == (1, 1, 2) and words.dtype == np.uint32
+    assert int(words[0, 0, 0]) == 0x7E014038 and int(words[0, 0, 1]) == 0x48300800
+    # the same bytes as a little-endian uint32 view of the plain scales
+    assert np.array_equal(words, plain.view("<u4"))
+
+
+def test_packed_u32_round_trip():
+    rng = np.random.default_rng(9)
+    plain = rng.integers(0, 256, size=(2, 256, 64), dtype=np.uint8)
+    assert np.array_equal(scale_layout.unpack_u32(scale_layout.pack_u32(plain)), plain)
+    with pytest.raises(ValueError):
+        scale_layout.pack_u32(plain[:, :, :6])
