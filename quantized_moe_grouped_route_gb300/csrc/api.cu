@@ -217,6 +217,7 @@ int qmoe_forward_kernel_count(int M, int top_k, int E, int sched) {
   if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
   if (M == 0) return 0;
   const long long P = (long long)M * top_k;
+  // the route (one kernel, or three above 8192 pairs), gather, FC1, FC2, combine
   return 4 + (route_scratch_bytes(P, E) > 0 ? 3 : 1);
 }
 

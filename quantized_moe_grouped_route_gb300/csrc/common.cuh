@@ -298,39 +298,6 @@ __device__ __forceinline__ void mma_bf16_ts_slab4x2(uint32_t pred, uint32_t d0, 
 }
 
 
-// Accumulator chains of a tile narrower than a third or so of its TMEM buffer: MMAs
-// into one accumulator wait for each other (~90 cycles each up to N = 128 whatever N),
-// so a narrow tile's 16-wide K slices are dealt round robin to `chains` accumulators
-// `stride` columns apart (slice s to chain s % chains), independent MMAs that overlap.
-// Issues the 4 MMAs of one 64-wide K slab: D[chain] (+)= A[a_tmem + 8j] * B[desc + 2j];
-// `ch` is the chain of the slab's first slice and `nsl` the slices issued so far in the
-// unit (a chain's first slice starts its accumulation); both are advanced.
-__device__ __forceinline__ void mma_bf16_ts_slab4_chains(uint32_t pred, uint32_t d_tmem,
-                                                         uint32_t stride, uint32_t chains,
-                                                         uint32_t& ch, uint32_t& nsl,
-                                                         uint32_t a_tmem, uint32_t desc_lo,
-                                                         uint32_t desc_hi, uint32_t idesc) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint64_t b = ((uint64_t)desc_hi << 32) | (desc_lo + 2u * j);
-    mma_bf16_ts_if(pred, d_tmem + ch * stride, a_tmem + 8u * j, b, idesc, nsl >= chains ? 1u : 0u);
-    ch = ch + 1 == chains ? 0u : ch + 1;
-    ++nsl;
-  }
-}
-
-// Chains for a tile of n16 (rows rounded up to 16) pairs in an accumulator buffer of
-// nmax columns: up to 4, each at least n16 columns wide (a multiple of 16); 1 for tiles
-// wider than 256 (their own two-chain split).
-__host__ __device__ __forceinline__ void acc_chains(int n16, int nmax, int& chains, int& stride) {
-  chains = 1;
-  stride = nmax;
-  if (n16 <= 256) {
-    chains = nmax / n16 < 4 ? nmax / n16 : 4;
-    stride = (nmax / chains) & ~15;
-  }
-}
-
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "

@@ -128,11 +128,13 @@ __host__ __device__ __forceinline__ uint32_t sk_range_start(unsigned long long n
   return (uint32_t)(n_steps * c / G);
 }
 // Whether the decode schedule splits units between CTAs: only when dealing whole units
-// (ceil(n_units / G) per CTA at most) would leave more than 1/32 of the CTAs' unit slots
-// idle; otherwise the partial sums cost more than the balance gains.
-__host__ __device__ __forceinline__ bool sk_split(long long n_units, unsigned int G) {
+// (ceil(n_units / G) per CTA at most) would leave more than two K steps per CTA idle on
+// average; below that the partial sums cost more than the balance gains (measured:
+// splitting gained 2% on FC1 of the M = 16 decode workload, 21.7 units of 28 steps per
+// CTA, and lost 10% on FC2 of the M = 1 one, 2.95 units of 12 steps).
+__host__ __device__ __forceinline__ bool sk_split(long long n_units, int nks, unsigned int G) {
   const long long waves = (n_units + G - 1) / G;
-  return waves * (long long)G * 32 > n_units * 33;
+  return (waves * (long long)G - n_units) * nks > 2LL * G;
 }
 // The CTA whose range holds global step g: the largest c with sk_range_start(c) <= g,
 // i.e. ceil((g + 1) G / n_steps) - 1.
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   const unsigned long long n_steps = (unsigned long long)n_units * (unsigned long long)nks;
   uint32_t g0 = 0, total = 0;
   if constexpr (BIN) {
-    if (sk_split(n_units, gridDim.x)) {
+    if (sk_split(n_units, nks, gridDim.x)) {
       g0 = sk_range_start(n_steps, blockIdx.x, gridDim.x);
       total = sk_range_start(n_steps, blockIdx.x + 1, gridDim.x) - g0;
     } else {  // whole units: a contiguous run of them per CTA, no partial sums
@@ -442,10 +444,6 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const uint32_t d_tmem = tmem + C::kAccCol0 + (ab * NMW + m) * NMAX;
       // this warp's first step of the segment: local step it + ks with (it + ks) % NMW == m
       const int ks0 = (m - (int)(it % NMW) + NMW) % NMW;
-      // narrow prefill tiles: K slices dealt to several accumulator chains
-      int chains = 1, cstride = NMAX;
-      if constexpr (!BIN) acc_chains(n16, NMAX, chains, cstride);
-      uint32_t ch = 0, nsl = 0;
       for (int ks = ks0; ks < len; ks += NMW) {
         const uint32_t sit = it + (uint32_t)ks;
         const int sl = sit % SL;
@@ -464,9 +462,6 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           if (NMAX > 256 && n16 > 256)
             mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0, b0, bdesc_hi, (256 * 128) >> 4,
                                 idesc, idesc2, acc);
-          else if (chains > 1)
-            mma_bf16_ts_slab4_chains(leader, d_tmem, cstride, chains, ch, nsl, a0, b0, bdesc_hi,
-                                     idesc);
           else
             mma_bf16_ts_slab4(leader, d_tmem, a0, b0, bdesc_hi, idesc, acc);
           tc_commit_if(leader, bempty0_u + sl * 8);
@@ -479,9 +474,6 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           if (NMAX > 256 && n16 > 256)
             mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0 + 32, b1, bdesc_hi,
                                 (256 * 128) >> 4, idesc, idesc2, 1u);
-          else if (chains > 1)
-            mma_bf16_ts_slab4_chains(leader, d_tmem, cstride, chains, ch, nsl, a0 + 32, b1,
-                                     bdesc_hi, idesc);
           else
             mma_bf16_ts_slab4(leader, d_tmem, a0 + 32, b1, bdesc_hi, idesc, 1u);
         } else {
@@ -645,34 +637,6 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         bool has[NMW];
 #pragma unroll
         for (int m = 0; m < NMW; ++m) has[m] = (m - (int)(it0 % NMW) + NMW) % NMW < nks;
-        int chains = 1, cstride = NMAX;
-        acc_chains(((rows + 15) >> 4) << 4, NMAX, chains, cstride);
-        if (chains > 1) {
-        // a tile on several accumulator chains: each 16-column chunk is the sum of the
-        // chains in the fixed order 0, 1, ..
-#pragma unroll 1
-        for (int kc = 0; 16 * kc < rows; ++kc) {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0.f;
-#pragma unroll 1
-          for (int c = 0; c < chains; ++c) {
-            uint32_t r[16];
-            tmem_ld_x16(tbase + c * cstride + 16 * kc, r);
-            tmem_wait_ld();
-            tmem_ld_ready(r);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(r[j]);
-          }
-          // (FC2: the chunk epilogue that broadcasts pair ids and weights by shuffles;
-          // the staged one would hold more registers than this kernel has)
-          if constexpr (FC1)
-            epilogue_chunk_fc1_tr<CLAMP>(p, v, lane, q, rb, start, rows, 16 * kc, gsc,
-                                         reinterpret_cast<uint8_t*>(st_pair));
-          else
-            epilogue_chunk_small<false>(p, v, lane, q, rb, start, rows, 16 * kc, gsc);
-        }
-        } else {
         // one batch body, reused (not unrolled: a smaller kernel, measurably faster)
 #pragma unroll 1
         for (int kc = 0; kc < NCH; kc += G) {
@@ -712,7 +676,6 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
             else
               epilogue_chunk_fc2_staged(p, v, lane, q, rb, rows, 16 * k, st_pair, st_w);
           }
-        }
         }
       }
       tc_fence_before();

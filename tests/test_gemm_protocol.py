@@ -284,18 +284,19 @@ def _cta_of(g, n_steps, G):
     return ((g + 1) * G + n_steps - 1) // n_steps - 1
 
 
-def _split(n_units, G):
+def _split(n_units, nks, G):
     waves = (n_units + G - 1) // G
-    return waves * G * 32 > n_units * 33
+    return (waves * G - n_units) * nks > 2 * G
 
 
 def test_stream_k_split_rule():
-    """Units are split between CTAs only where whole units would idle more than 1/32 of
-    the last wave: the decode workloads' FC1 (384 and 3200 units on 152 CTAs) split,
-    their FC2 (448 and 5600 units) do not."""
-    assert _split(384, 152) and _split(3200, 152)
-    assert not _split(448, 152) and not _split(5600, 152)
-    assert not _split(152, 152) and _split(153, 152) and _split(1, 152)
+    """Units are split between CTAs only where whole units would leave more than two K
+    steps per CTA idle on average: the decode workloads' FC1 (384 units of 28 steps,
+    3300 of 28) split, their FC2 (448 of 12, 5600 of 8) do not."""
+    assert _split(384, 28, 152) and _split(3300, 28, 152)
+    assert not _split(448, 12, 152) and not _split(5600, 8, 152)
+    assert not _split(152, 28, 152) and _split(153, 28, 152) and _split(1, 28, 152)
+    assert not _split(1, 1, 152)
 
 
 @pytest.mark.parametrize("n_units,G", [(448, 152), (5600, 152), (7, 3), (1, 1)])
