@@ -76,6 +76,15 @@ def _bind(lib):
     lib.qo_forward_h.restype = i32
     lib.qo_forward_h.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, i32, i32, P, i64, P, P,
                                  i32, P, P, P]
+    lib.qo_e4m3_rne.restype = ctypes.c_uint8
+    lib.qo_e4m3_rne.argtypes = [ctypes.c_double]
+    lib.qo_e2m1_nearest.restype = i32
+    lib.qo_e2m1_nearest.argtypes = [ctypes.c_double]
+    lib.qo_nvfp4_row.restype = None
+    lib.qo_nvfp4_row.argtypes = [P, i64]
+    lib.qo_forward_w4a4.restype = i32
+    lib.qo_forward_w4a4.argtypes = [P, P, P, P, P, P, P, P, P, i64, i64, i64, i32, i32, P, i64, P,
+                                    P, i32]
     lib.qo_max_threads.restype = i32
     lib.qo_max_threads.argtypes = []
     return lib
@@ -189,6 +198,53 @@ def forward(x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, tokens=None,
         res.append({"h": hout, "compared": int(stats[0]), "flipped": int(stats[1]),
                     "outside": int(stats[2])})
     return tuple(res) if len(res) > 1 else out
+
+
+def e4m3_rne(v: float, lib=None) -> int:
+    """E4M3 byte nearest to v >= 0, ties to even, saturating at 448."""
+    return (lib or _load()).qo_e4m3_rne(v)
+
+
+def e2m1_nearest(r: float, lib=None) -> int:
+    """E2M1 code nearest to r, ties to the even mantissa, saturating at 6."""
+    return (lib or _load()).qo_e2m1_nearest(r)
+
+
+def nvfp4_row(v, lib=None) -> np.ndarray:
+    """NVFP4 encode-decode of activation rows (last axis, a multiple of 16), as the W4A4
+    variant quantizes x and h (see qo_forward_w4a4)."""
+    a = np.array(v, dtype=np.float64, copy=True)
+    rows = a.reshape(-1, a.shape[-1])
+    for r in rows:
+        (lib or _load()).qo_nvfp4_row(_ptr(r), r.size)
+    return rows.reshape(a.shape)
+
+
+def forward_w4a4(x, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, tokens=None,
+                 nthreads: int | None = None, lib=None, return_f64: bool = False):
+    """The W4A4 variant of the layer (x and h quantized to NVFP4 per row, see
+    qo_forward_w4a4) on the CPU in fp64; bf16 bits [n_tokens][H] (and the fp64 values)."""
+    lib = lib or _load()
+    xb = _np(x, np.uint16)
+    M, H = xb.shape
+    E = int(np.asarray(w13.shape)[0])
+    I = int(w13.shape[1]) // 2
+    top_k = int(topk_ids.shape[1])
+    a13, b13, c13 = _np(w13, np.uint8), _np(s13, np.uint8), _np(gs13, np.float32)
+    a2, b2, c2 = _np(w2, np.uint8), _np(s2, np.uint8), _np(gs2, np.float32)
+    ids, wts = _np(topk_ids, np.int32), _np(topk_weights, np.float32)
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    n = M if tok is None else tok.size
+    out = np.zeros((n, H), np.uint16)
+    out64 = np.zeros((n, H), np.float64) if return_f64 else None
+    rc = lib.qo_forward_w4a4(_ptr(xb), _ptr(a13), _ptr(b13), _ptr(c13), _ptr(a2), _ptr(b2),
+                             _ptr(c2), _ptr(ids), _ptr(wts), M, H, I, E, top_k,
+                             _ptr(tok) if tok is not None else None, n, _ptr(out),
+                             _ptr(out64) if out64 is not None else None,
+                             nthreads or lib.qo_max_threads())
+    if rc < 0:
+        raise ValueError(f"qo_forward_w4a4 failed: {rc}")
+    return (out, out64) if return_f64 else out
 
 
 def max_threads(lib=None) -> int:

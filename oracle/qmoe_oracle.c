@@ -359,6 +359,141 @@ int qo_forward(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const 
                       n_tokens, out_bf16, out_f64, nthreads, NULL, NULL, NULL);
 }
 
+/*
+ * W4A4 variant (tilelang_kernels.py page, module docstring: the native E2M1 x UE4M3
+ * block-scaled MMA, which needs the activations in NVFP4 as well).  The pages do not say
+ * how activations are quantized; the reading taken is the NVFP4 encoding the workload
+ * recipe gives for the weights, applied to each activation row on its own (the row's
+ * values are its K dimension):
+ *   g     = amax of the row / (6 * 448)            (1 when the row is all zero)
+ *   scale = E4M3, round to nearest even, of (amax of the 16-block) / 6 / g
+ *   code  = nearest E2M1 value of v / (scale * g), ties to the even mantissa, at most 6
+ *   v'    = E2M1(code) * E4M3(scale) * g
+ * x is quantized per token, h (after its bf16 rounding) per (token, slot) pair; the rest
+ * of the layer is as in qo_forward.
+ */
+
+/* E4M3 byte nearest to v >= 0 (ties to even), saturating at 448. */
+uint8_t qo_e4m3_rne(double v) {
+  if (!(v > 0.0)) return 0;
+  if (v >= 448.0) return 0x7E;
+  int ex;
+  frexp(v, &ex); /* v in [2^(ex-1), 2^ex) */
+  int e = ex - 1;
+  if (e < -6) e = -6;                 /* subnormal range: spacing 2^-9 */
+  double q = ldexp(1.0, e - 3);       /* 3 mantissa bits */
+  double r = rint(v / q) * q;         /* nearest, ties to even */
+  if (r >= 448.0) return 0x7E;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(r / ldexp(1.0, -9)); /* subnormal: m * 2^-9 */
+  int ex2;
+  double f = frexp(r, &ex2); /* r = f * 2^ex2, f in [0.5, 1) */
+  int E = ex2 - 1 + 7;
+  int m = (int)((f * 2.0 - 1.0) * 8.0);
+  return (uint8_t)((E << 3) | m);
+}
+
+/* E2M1 code (sign in bit 3) nearest to r, ties to the even mantissa, saturating at 6;
+ * a result of -0 is +0. */
+int qo_e2m1_nearest(double r) {
+  double a = fabs(r);
+  int best = 0;
+  double bd = fabs(a - kE2M1Mag[0]);
+  for (int c = 1; c < 8; ++c) {
+    double d = fabs(a - kE2M1Mag[c]);
+    if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      bd = d;
+    }
+  }
+  return (r < 0.0 && best != 0) ? (best | 8) : best;
+}
+
+/* NVFP4 encode-decode of one activation row of n values (n % 16 == 0), in place. */
+void qo_nvfp4_row(double* v, int64_t n) {
+  double amax = 0.0;
+  for (int64_t i = 0; i < n; ++i)
+    if (fabs(v[i]) > amax) amax = fabs(v[i]);
+  double g = amax / (6.0 * 448.0);
+  if (g == 0.0) g = 1.0;
+  for (int64_t b = 0; b < n; b += 16) {
+    double bmax = 0.0;
+    for (int64_t i = b; i < b + 16; ++i)
+      if (fabs(v[i]) > bmax) bmax = fabs(v[i]);
+    double sc = qo_dec_e4m3(qo_e4m3_rne(bmax / 6.0 / g));
+    for (int64_t i = b; i < b + 16; ++i)
+      v[i] = sc > 0.0 ? qo_dec_e2m1(qo_e2m1_nearest(v[i] / (sc * g))) * sc * g : 0.0;
+  }
+}
+
+int qo_forward_w4a4(const uint16_t* x, const uint8_t* w13, const uint8_t* s13, const float* gs13,
+                    const uint8_t* w2, const uint8_t* s2, const float* gs2, const int32_t* ids,
+                    const float* topk_w, int64_t M, int64_t H, int64_t I, int E, int top_k,
+                    const int64_t* tokens, int64_t n_tokens, uint16_t* out_bf16, double* out_f64,
+                    int nthreads) {
+  if (M < 0 || H < 16 || I < 16 || H % 16 || I % 16 || E < 1 || top_k < 1) return QO_ERR_ARG;
+  if (tokens == NULL) n_tokens = M;
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    int64_t m = tokens ? tokens[t] : t;
+    if (m < 0 || m >= M) return QO_ERR_ARG;
+  }
+  int bad_id = 0, nan_scale = 0;
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+    double* g = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* h = (double*)malloc(sizeof(double) * (size_t)I);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n_tokens; ++t) {
+      int64_t m = tokens ? tokens[t] : t;
+      for (int64_t hh = 0; hh < H; ++hh) xq[hh] = qo_bf16_to_double(x[(size_t)m * H + hh]);
+      qo_nvfp4_row(xq, H);
+      for (int64_t j = 0; j < H; ++j) acc[j] = 0.0;
+      for (int k = 0; k < top_k; ++k) {
+        int e = ids[m * top_k + k];
+        if (e < 0) {
+          continue;  /* no expert in this slot */
+        } else if (e >= E) {
+          bad_id = 1;
+          continue;
+        }
+        const uint8_t* we = w13 + (int64_t)e * (2 * I) * (H / 2);
+        const uint8_t* se = s13 + (int64_t)e * (2 * I) * (H / 16);
+        for (int64_t n = 0; n < 2 * I; ++n) {
+          double sum = 0.0;
+          for (int64_t hh = 0; hh < H; ++hh) sum += xq[hh] * wq(we, se, H, n, hh);
+          g[n] = sum * (double)gs13[e];
+        }
+        for (int64_t i = 0; i < I; ++i) {
+          const double upv = g[i], gatev = g[I + i];
+          const double sg = gatev / (1.0 + exp(-gatev));
+          h[i] = qo_bf16_to_double(qo_bf16_rne(sg * upv));
+        }
+        qo_nvfp4_row(h, I);
+        const uint8_t* w2e = w2 + (int64_t)e * H * (I / 2);
+        const uint8_t* s2e = s2 + (int64_t)e * H * (I / 16);
+        for (int64_t j = 0; j < H; ++j) {
+          double sum = 0.0;
+          for (int64_t i = 0; i < I; ++i) sum += h[i] * wq(w2e, s2e, I, j, i);
+          acc[j] += (double)topk_w[m * top_k + k] * ((double)gs2[e] * sum);
+        }
+      }
+      for (int64_t j = 0; j < H; ++j) {
+        if (isnan(acc[j])) nan_scale = 1;
+        out_bf16[t * H + j] = qo_bf16_rne(acc[j]);
+        if (out_f64) out_f64[t * H + j] = acc[j];
+      }
+    }
+    free(xq);
+    free(g);
+    free(h);
+    free(acc);
+  }
+  if (nan_scale) return QO_ERR_NAN_SCALE;
+  return bad_id ? QO_WARN_BAD_ID : QO_OK;
+}
+
 /* Number of threads OpenMP would use by default (the host's cores). */
 int qo_max_threads(void) {
 #ifdef _OPENMP

@@ -88,3 +88,58 @@ def forward(x_bf16_bits, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights, sw
             sel = slots == k
             np.add.at(acc, toks[sel], contrib[sel])
     return round_bf16(acc), acc
+
+
+def nvfp4_rows(v: np.ndarray) -> np.ndarray:
+    """NVFP4 encode-decode of activation rows (last axis, a multiple of 16) as the W4A4
+    variant defines it: per row g = amax / (6 * 448) (1 for an all-zero row); per
+    16-block the E4M3 scale nearest (ties to even) to blockamax / 6 / g; each value the
+    E2M1 value nearest (ties to the even mantissa, at most 6) to v / (scale * g), times
+    scale * g.  Written with NumPy array operations."""
+    v = np.asarray(v, dtype=np.float64)
+    shp = v.shape
+    rows = v.reshape(-1, shp[-1])
+    amax = np.abs(rows).max(axis=1, keepdims=True)
+    g = np.where(amax > 0, amax / (6.0 * 448.0), 1.0)
+    blk = rows.reshape(rows.shape[0], -1, 16)
+    bmax = np.abs(blk).max(axis=2, keepdims=True)
+    t = bmax / 6.0 / g[:, :, None]
+    # E4M3: 3 mantissa bits, exponents down to -6 (subnormal spacing 2^-9), max 448
+    e = np.floor(np.log2(np.where(t > 0, t, 1.0)))
+    q = np.exp2(np.maximum(e, -6.0) - 3.0)
+    sc = np.minimum(np.rint(t / q) * q, 448.0)
+    sc = np.where(t > 0, sc, 0.0)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    r = np.abs(blk) / np.where(sc > 0, sc * g[:, :, None], 1.0)
+    d = np.abs(r[..., None] - mags)                      # distance to each magnitude
+    # nearest; on a tie the even code index (even mantissa) wins: add a tiny bias to odd
+    best = np.argmin(d + (np.arange(8) % 2) * 1e-12 * np.maximum(r[..., None], 1.0), axis=-1)
+    out = np.sign(blk) * mags[best] * sc * g[:, :, None]
+    out = np.where(sc > 0, out, 0.0)
+    return out.reshape(shp)
+
+
+def forward_w4a4(x_bf16_bits, w13, s13, gs13, w2, s2, gs2, topk_ids, topk_weights):
+    """The W4A4 variant: x quantized per token and h (after its bf16 rounding) per pair
+    with nvfp4_rows, otherwise as forward()."""
+    x = (np.asarray(x_bf16_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    x = nvfp4_rows(x.astype(np.float64))
+    M, H = x.shape
+    E = w13.shape[0]
+    top_k = topk_ids.shape[1]
+    I = w13.shape[1] // 2
+    acc = np.zeros((M, H), np.float64)
+    for e in range(E):
+        toks, slots = np.nonzero(topk_ids == e)
+        if toks.size == 0:
+            continue
+        W13 = dequant(w13[e], s13[e]) * np.float64(gs13[e])
+        W2 = dequant(w2[e], s2[e]) * np.float64(gs2[e])
+        g = x[toks] @ W13.T
+        up, gate = g[:, :I], g[:, I:]
+        h = nvfp4_rows(round_bf16(gate / (1.0 + np.exp(-gate)) * up))
+        contrib = (h @ W2.T) * topk_weights[toks, slots].astype(np.float64)[:, None]
+        for k in range(top_k):
+            sel = slots == k
+            np.add.at(acc, toks[sel], contrib[sel])
+    return round_bf16(acc), acc

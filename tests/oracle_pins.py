@@ -645,7 +645,107 @@ def pin_swiglu_limit_numpy_twin(lib):
         assert np.array_equal(oracle.bf16_bits_to_float(out), twin_bf)
 
 
+# ---------------------------------------------------------------------------
+# W4A4 variant: the activation quantizer and the layer
+# ---------------------------------------------------------------------------
+
+def _e2m1_brute(r: float) -> int:
+    """Nearest E2M1 code by enumeration; ties to the even code (even mantissa)."""
+    best = min(range(8), key=lambda c: (abs(abs(r) - E2M1_TABLE[c]), c & 1))
+    return best | 8 if (r < 0 and best) else best
+
+
+def pin_e4m3_rne(lib):
+    """E4M3 rounding (round to nearest, ties to even, saturating at 448) against torch's
+    float8_e4m3fn conversion of fp32-exact values, every E4M3 value onto itself, and
+    the midpoints between neighbours onto the even one."""
+    g = torch.Generator().manual_seed(41)
+    v = torch.exp2(torch.empty(3000).uniform_(-12, 8.8, generator=g)).clamp(max=448.0)
+    want = v.to(torch.float8_e4m3fn).view(torch.uint8).int().tolist()
+    for a, w in zip(v.double().tolist(), want):
+        assert oracle.e4m3_rne(a, lib) == w, (a, oracle.e4m3_rne(a, lib), w)
+    vals = [oracle.dec_e4m3(b, lib) for b in range(0x7F)]
+    for b in range(0x7F):
+        assert oracle.e4m3_rne(vals[b], lib) == b
+    for b in range(0x7E):
+        mid = 0.5 * (vals[b] + vals[b + 1])
+        assert oracle.e4m3_rne(mid, lib) == (b if b % 2 == 0 else b + 1), b
+    assert oracle.e4m3_rne(1e9, lib) == 0x7E and oracle.e4m3_rne(0.0, lib) == 0
+
+
+def pin_e2m1_nearest(lib):
+    vals = [k / 16.0 for k in range(-128, 129)] + [7.0, -9.5, 1e-3, 5.999, 2.4999]
+    for r in vals:
+        assert oracle.e2m1_nearest(r, lib) == _e2m1_brute(r), r
+
+
+def _nvfp4_row_brute(v):
+    """Row quantizer from its definition, with torch's float8 conversion for the E4M3
+    scale and enumeration for the codes."""
+    v = np.asarray(v, dtype=np.float64)
+    amax = float(np.abs(v).max())
+    g = amax / (6.0 * 448.0) if amax > 0 else 1.0
+    out = np.zeros_like(v)
+    for b in range(0, v.size, 16):
+        t = float(np.abs(v[b:b + 16]).max()) / 6.0 / g
+        sc = float(torch.tensor([min(t, 448.0)], dtype=torch.float64).float()
+                   .to(torch.float8_e4m3fn).float())
+        for i in range(b, b + 16):
+            if sc > 0:
+                c = _e2m1_brute(v[i] / (sc * g))
+                out[i] = (-1.0 if c & 8 else 1.0) * E2M1_TABLE[c & 7] * sc * g
+    return out
+
+
+def pin_nvfp4_row(lib):
+    """The W4A4 activation quantizer: against the brute-force statement on random rows
+    (with an all-zero block and an outlier), a fixed point on rows already in NVFP4,
+    and equivariance under scaling by powers of two."""
+    rng = np.random.default_rng(43)
+    for n, scale in ((64, 1.0), (128, 3e-3), (256, 40.0)):
+        v = rng.standard_normal(n) * scale
+        v[16:32] = 0.0
+        v[5] *= 30.0
+        v = v.astype(np.float32).astype(np.float64)
+        got = oracle.nvfp4_row(v, lib)
+        assert np.array_equal(got, _nvfp4_row_brute(v)), n
+        # exactly representable: codes times an E4M3 scale times g, each block holding a
+        # code of magnitude 6 (so its amax / 6 / g is its scale), amax 6 * 448 * g
+        g = 0.01
+        codes = rng.integers(0, 16, size=n)
+        codes[::16] = 7
+        scales = np.array([oracle.dec_e4m3(int(b), lib) for b in rng.integers(40, 110, size=n // 16)])
+        scales[0] = 448.0
+        rep = np.array([oracle.dec_e2m1(int(c), lib) for c in codes]) * np.repeat(scales, 16) * g
+        rep[0] = 6.0 * 448.0 * g
+        assert np.array_equal(oracle.nvfp4_row(rep, lib), rep)
+        for k in (-7, 5):
+            assert np.array_equal(oracle.nvfp4_row(v * 2.0 ** k, lib), got * 2.0 ** k)
+    assert not oracle.nvfp4_row(np.zeros(32), lib).any()
+
+
+def pin_w4a4_numpy_twin(lib):
+    """The W4A4 layer against the NumPy statement (ref_numpy.forward_w4a4)."""
+    from oracle import ref_numpy
+    for seed in (44, 45):
+        t = _random_layer(seed, M=5, H=64, I=48, E=3, top_k=2)
+        t["topk_ids"][2, 1] = -1
+        out, f64 = oracle.forward_w4a4(t["x"], t["w13"], t["s13"], t["gs13"], t["w2"], t["s2"],
+                                       t["gs2"], t["topk_ids"], t["topk_weights"], lib=lib,
+                                       nthreads=2, return_f64=True)
+        twin_bf, twin64 = ref_numpy.forward_w4a4(t["x"], t["w13"], t["s13"], t["gs13"], t["w2"],
+                                                 t["s2"], t["gs2"], t["topk_ids"],
+                                                 t["topk_weights"])
+        assert np.allclose(f64, twin64, rtol=1e-11, atol=1e-14)
+        assert np.array_equal(oracle.bf16_bits_to_float(out), twin_bf)
+        # and it is a different layer from W4A16 (the quantization is not a no-op)
+        w4a16 = oracle.forward(t["x"], t["w13"], t["s13"], t["gs13"], t["w2"], t["s2"],
+                               t["gs2"], t["topk_ids"], t["topk_weights"], lib=lib, nthreads=2)
+        assert not np.array_equal(out, w4a16)
+
+
 ALL_PINS = [pin_e2m1, pin_e4m3, pin_bf16_decode, pin_bf16_round, pin_route, pin_zero_weights,
             pin_single_nibble, pin_h_given, pin_h_bound_production, pin_permutation_blocks, pin_subnormal_scale, pin_token_permutation,
             pin_duplicate_expert, pin_weight_linearity, pin_numpy_twin, pin_tiny_config,
-            pin_swiglu_limit, pin_swiglu_limit_infinite, pin_swiglu_limit_numpy_twin]
+            pin_swiglu_limit, pin_swiglu_limit_infinite, pin_swiglu_limit_numpy_twin,
+            pin_e4m3_rne, pin_e2m1_nearest, pin_nvfp4_row, pin_w4a4_numpy_twin]

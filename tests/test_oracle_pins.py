@@ -40,6 +40,13 @@ MUTANTS = {
     "h_bound_worst_case_wide": ("ga[n] = fabs((double)gs13[e]) * 2.0 * u * err;",
                                 "ga[n] = fabs((double)gs13[e]) * 2.0 * u * err * 200.0;"),
     "h_bound_first_order_only": ("1.1 * (fabs(up) + d_up) * d_gate", "1.1 * fabs(up) * d_gate"),
+    "w4a4_e4m3_ties_up": ("double r = rint(v / q) * q;         /* nearest, ties to even */",
+                          "double r = floor(v / q + 0.5) * q;"),
+    "w4a4_e2m1_ties_odd": ("(d == bd && (c & 1) == 0 && (best & 1) == 1)", "(d == bd && (c & 1) == 1)"),
+    "w4a4_global_scale": ("double g = amax / (6.0 * 448.0);\n  if (g == 0.0) g = 1.0;\n  for (int64_t b",
+                          "double g = amax / 448.0;\n  if (g == 0.0) g = 1.0;\n  for (int64_t b"),
+    "w4a4_h_not_quantized": ("        qo_nvfp4_row(h, I);\n", "\n"),
+    "w4a4_x_not_quantized": ("      qo_nvfp4_row(xq, H);\n", "\n"),
     "h_flip_uncounted": ("if (given != h[i]) n_flip += 1;", ";"),
     "routing_weight_dropped": ("acc[j] += (double)topk_w[m * top_k + k] * y;", "acc[j] += y;"),
     "e2m1_sign_dropped": ("return (code & 8) ? -m : m;", "return m;"),
