@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--sched", choices=["auto", "decode", "prefill", "prefill_pair"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true",
-                    help="skip the untimed clock-sampling soak (for profiler launch lists)")
+                    help="skip the untimed soak before each timed region (for profiler runs)")
     ap.add_argument("--no-extra-configs", action="store_true",
                     help="time only the headline workload (not the other decode / prefill ones)")
     return ap.parse_args()
@@ -263,7 +263,7 @@ def roofline_entry(cfg, alg, stage_ms, decode, sched_name, peaks):
 
 
 def time_workload(cfg, sched, K, warmup, dev, rank, world, barrier, token_seed=None,
-                  keep_plain=False):
+                  keep_plain=False, soak=True):
     """Build one workload, warm up, time K forwards (one region, CUDA events on the
     launching stream), then K more with the library's stage events for per-kernel times.
     Returns everything the JSON line reports about it, plus the objects e2e needs."""
@@ -305,6 +305,13 @@ def time_workload(cfg, sched, K, warmup, dev, rank, world, barrier, token_seed=N
     rc, flags = qmoe.qmoe_read_error(ws)
     if rc != 0:
         raise RuntimeError(f"{cfg.name}: device error word after warm-up: rc={rc} flags={flags}")
+    # an untimed soak of the same steps right before the timed region, so that the clock
+    # sampler (every 100 ms) sees this workload's load even when the region is short
+    soak0 = time.time()
+    while soak and time.time() - soak0 < 0.5:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     for row in evs:  # torch creates the CUDA event on first record
         for ev in row:
@@ -336,7 +343,7 @@ def time_workload(cfg, sched, K, warmup, dev, rank, world, barrier, token_seed=N
                            f"flags={flags}")
     return {"li": li, "layer": layer, "ws": ws, "out": out, "stream": stream, "ms": ms,
             "stage_ms": stage_ms, "step_median_ms": step_median, "repack_ms": repack_ms,
-            "window": (wall0, wall1)}
+            "window": (soak0 if soak else wall0, wall1)}
 
 
 def ours_arm(args, rank, world, local):
@@ -363,20 +370,9 @@ def ours_arm(args, rank, world, local):
 
     sampler = ClockSampler(local)
     sampler.start()
-    if not args.no_soak:  # let the sampler see the GPU under this load before the timed region
-        w = time_workload(cfg, sched, 20, args.warmup, dev, rank, world, barrier,
-                          token_seed=cfg.seed + 1000 * rank)
-        t_soak = time.time()
-        while time.time() - t_soak < 0.6:
-            for _ in range(20):
-                qmoe.moe_nvfp4_forward(w["li"].x, w["layer"].w13c, w["layer"].w13s,
-                                       w["layer"].gs13, w["layer"].w2c, w["layer"].w2s,
-                                       w["layer"].gs2, w["li"].topk_ids, w["li"].topk_weights,
-                                       w["out"], H=H, I=I, E=E, sched=sched, workspace=w["ws"])
-            torch.cuda.synchronize()
-        del w
     main = time_workload(cfg, sched, args.steps, args.warmup, dev, rank, world, barrier,
-                         token_seed=cfg.seed + 1000 * rank, keep_plain=True)
+                         token_seed=cfg.seed + 1000 * rank, keep_plain=True,
+                         soak=not args.no_soak)
     ms = max_over_ranks(main["ms"], world, dev)
     li, layer, out, stream = main["li"], main["layer"], main["out"], main["stream"]
 
@@ -430,7 +426,7 @@ def ours_arm(args, rank, world, local):
         for name in EXTRA_CONFIGS:
             c = config_by_name(name)
             r = time_workload(c, qmoe.QMOE_SCHED_AUTO, steps_x, args.warmup, dev, rank, world,
-                              barrier)
+                              barrier, soak=not args.no_soak)
             a = algorithmic_bytes(c, r["li"].topk_ids.cpu())
             dec = is_decode(qmoe, qmoe.QMOE_SCHED_AUTO, c.M, c.top_k, c.E)
             sn = "decode" if dec else "prefill"

@@ -110,3 +110,29 @@ def test_prefill_pair_schedule_full_size(cfg):
         "two-SM schedule not deterministic"
     toks = forced_tokens(li, s, n_random=32, seed=cfg.seed)
     check_layer(li, outs[1], layer._ws, s, tokens=toks, what=f"{cfg.name} two-SM")
+
+
+@pytest.mark.parametrize("cfg", [CONFIGS[1], CONFIGS[3]], ids=lambda c: c.name)
+def test_forward_replays_from_a_cuda_graph(cfg):
+    """The forward is stream work only (a memset and kernel launches, no host sync), so
+    it captures into a CUDA graph; replays give the eager call's output bit for bit."""
+    li = make_inputs(cfg, "cuda")
+    layer = qmoe.NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
+    ref = layer(li.x, li.topk_ids, li.topk_weights).clone()
+    torch.cuda.synchronize()
+    out = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer(li.x, li.topk_ids, li.topk_weights, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer(li.x, li.topk_ids, li.topk_weights, out=out)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    rc, flags = qmoe.qmoe_read_error(layer._ws)
+    assert rc == 0 and flags == 0
