@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "dequant.cuh"
 #include "launch.h"
 
 namespace qmoe {
@@ -358,7 +359,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
                                n_tiles, err, ws + L.route_scratch, s);
   if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
   const bool pdl = forward_uses_pdl(rsched);
-  e = launch_gather(x_dev, sorted_pair, offsets + E, top_k, H, P, xs, sms, s, pdl);
+  e = launch_gather(x_dev, pair_pos, M, top_k, H, xs, sms, s, pdl);
   if (e != cudaSuccess || !mark(2)) return QMOE_ERR_CUDA;
 
   GemmParams p1;
@@ -374,6 +375,9 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p1.I = I;
   p1.swiglu_limit = swiglu_limit;
   p1.err = err;
+  p1.dq_mul[0] = dequant_mul().m64;
+  p1.dq_mul[1] = dequant_mul().m8;
+  p1.dq_mul[2] = dequant_mul().m4;
   p1.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
   p1.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt1);
   e = launch_gemm(GemmKind::kFc1, rsched, map_x, p1, sms, s);
@@ -393,6 +397,9 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p2.topk_w = topk_weights_dev;
   p2.H = H;
   p2.err = err;
+  p2.dq_mul[0] = dequant_mul().m64;
+  p2.dq_mul[1] = dequant_mul().m8;
+  p2.dq_mul[2] = dequant_mul().m4;
   p2.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
   p2.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt2);
   e = launch_gemm(GemmKind::kFc2, rsched, map_h, p2, sms, s);

@@ -522,6 +522,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // bits flip on each wrap.
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
     uint32_t pos = (g0 + (uint32_t)grp) % (uint32_t)nks;  // step of the current one within its unit
+    const DequantMul dqm{p.dq_mul[0], p.dq_mul[1], p.dq_mul[2]};
     for (uint32_t it = grp; it < total; it += DG) {
       const int nh = (KS == 2 && pos == (uint32_t)nks - 1) ? last_halves : KS;
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;
@@ -555,10 +556,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint32_t o[16];
-            dequant8(cw[h][kk].x, sv[2 * kk], o + 0);
-            dequant8(cw[h][kk].y, sv[2 * kk], o + 4);
-            dequant8(cw[h][kk].z, sv[2 * kk + 1], o + 8);
-            dequant8(cw[h][kk].w, sv[2 * kk + 1], o + 12);
+            dequant8(cw[h][kk].x, sv[2 * kk], o + 0, dqm);
+            dequant8(cw[h][kk].y, sv[2 * kk], o + 4, dqm);
+            dequant8(cw[h][kk].z, sv[2 * kk + 1], o + 8, dqm);
+            dequant8(cw[h][kk].w, sv[2 * kk + 1], o + 12, dqm);
             tmem_st_x16(ta + h * 64 + kk * 16, o);
           }
           tmem_wait_st();

@@ -362,6 +362,7 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
     const int grp = (warp - kDequantWarp0) >> 2;
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    const DequantMul dqm{p.dq_mul[0], p.dq_mul[1], p.dq_mul[2]};
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
     for (uint32_t it = grp; it < total; it += DG) {
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;
@@ -382,10 +383,10 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t o[16];
-        dequant8(cw[kk].x, sv[2 * kk], o + 0);
-        dequant8(cw[kk].y, sv[2 * kk], o + 4);
-        dequant8(cw[kk].z, sv[2 * kk + 1], o + 8);
-        dequant8(cw[kk].w, sv[2 * kk + 1], o + 12);
+        dequant8(cw[kk].x, sv[2 * kk], o + 0, dqm);
+        dequant8(cw[kk].y, sv[2 * kk], o + 4, dqm);
+        dequant8(cw[kk].z, sv[2 * kk + 1], o + 8, dqm);
+        dequant8(cw[kk].w, sv[2 * kk + 1], o + 12, dqm);
         tmem_st_x16(ta + kk * 16, o);
       }
       tmem_wait_st();

@@ -22,9 +22,9 @@ cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int 
                           int scale_layout, uint8_t* out_codes, uint8_t* out_scales,
                           cudaStream_t stream);
 // pdl: launch with programmatic stream serialization (see pdl_attribute)
-cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
-                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream,
-                          bool pdl);
+// xs[pair_pos[i]] = x[i / top_k] for every routed pair i (pair_pos[i] >= 0)
+cudaError_t launch_gather(const void* x, const int32_t* pair_pos, int M, int top_k, int H,
+                          void* xs, int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
                            void* out, int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_selftest_dequant(uint16_t* out, cudaStream_t stream);
@@ -54,6 +54,7 @@ struct GemmParams {
   // quarter), zero at launch
   float* sk_part;
   int* sk_cnt;
+  uint32_t dq_mul[3];  // the dequant's multipliers 64, 8, 4 (dequant_mul), as runtime values
 };
 
 // Largest grid of the decode schedule (its partial buffer has a slot pair per CTA).

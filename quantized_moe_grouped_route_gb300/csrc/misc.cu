@@ -86,28 +86,42 @@ __global__ void repack_scales_kernel(const uint8_t* __restrict__ s, int E, int N
   }
 }
 
-// xs[pos] = x[sorted_pair[pos] / top_k] for the n_valid routed pairs, 16-byte chunks.
-// Work items are (row, segment of 256 chunks) taken one per warp: the row's source is
-// looked up once per item, and small batches still spread over many warps.
-__global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_pair,
-                              const int32_t* __restrict__ n_valid_p, int top_k, int chunks,
-                              uint4* __restrict__ xs) {
+// xs[pair_pos[m * top_k + k]] = x[m] for every routed pair, 16-byte chunks.  Work items
+// are (token, segment of 256 chunks) taken one per warp: the warp reads its segment of
+// the token's row once (eight 16-byte chunks per lane) and writes it to the position of
+// each of the token's routed pairs, so x is read in one pass however many of its slots
+// a token routes (reading it per pair in expert order re-read each row top_k times,
+// mostly from L2 but not always).
+__global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ pair_pos,
+                              int M, int top_k, int chunks, uint4* __restrict__ xs) {
   grid_dep_wait();    // the route's outputs
   grid_dep_launch();  // FC1 may start streaming weights
-  constexpr int kSeg = 256;
+  constexpr int kSeg = 256, kPer = kSeg / 32;
   const int nseg = (chunks + kSeg - 1) / kSeg;
-  const long long items = (long long)(*n_valid_p) * nseg;
+  const long long items = (long long)M * nseg;
   const int lane = threadIdx.x & 31;
   const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long it = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < items;
        it += warps) {
-    const int pos = (int)(it / nseg);
-    const int c0 = (int)(it - (long long)pos * nseg) * kSeg;
-    const int c1 = min(chunks, c0 + kSeg);
-    const int tok = sorted_pair[pos] / top_k;
-    const uint4* src = x + (size_t)tok * chunks;
-    uint4* dst = xs + (size_t)pos * chunks;
-    for (int c = c0 + lane; c < c1; c += 32) dst[c] = src[c];
+    const int m = (int)(it / nseg);
+    const int c0 = (int)(it - (long long)m * nseg) * kSeg;
+    const uint4* src = x + (size_t)m * chunks;
+    uint4 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int c = c0 + lane + 32 * j;
+      if (c < chunks) v[j] = src[c];
+    }
+    for (int k = 0; k < top_k; ++k) {
+      const int pos = pair_pos[(size_t)m * top_k + k];
+      if (pos < 0) continue;
+      uint4* dst = xs + (size_t)pos * chunks;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int c = c0 + lane + 32 * j;
+        if (c < chunks) dst[c] = v[j];
+      }
+    }
   }
 }
 
@@ -151,8 +165,9 @@ __global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* _
   }
 }
 
-// Every (code, scale) pair through the GEMM's dequant path.
-__global__ void selftest_dequant_kernel(uint16_t* __restrict__ out) {
+// Every (code, scale) pair through the GEMM's dequant path (with its multipliers passed
+// in at run time, as the GEMM gets them).
+__global__ void selftest_dequant_kernel(uint16_t* __restrict__ out, DequantMul dqm) {
   const int sb = blockIdx.x;  // scale byte
   const int c = threadIdx.x;  // 0..15
   if (c >= 16) return;
@@ -161,7 +176,7 @@ __global__ void selftest_dequant_kernel(uint16_t* __restrict__ out) {
   const int pos = c & 7;
   const uint32_t plain = (uint32_t)c << (4 * pos);
   uint32_t o[4];
-  dequant8(pack_codes8(plain), s2, o);
+  dequant8(pack_codes8(plain), s2, o, dqm);
   const uint32_t word = o[pos >> 1];
   const uint16_t v = (pos & 1) ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFF);
   // undo the 2^-7 the kernels fold into the epilogue: multiply by 128 exactly
@@ -209,20 +224,19 @@ cudaError_t launch_repack(const uint8_t* w, const uint8_t* s, int E, int N, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const void* x, const int32_t* sorted_pair, const int32_t* n_valid,
-                          int top_k, int H, int P, void* xs, int num_sms, cudaStream_t stream,
-                          bool pdl) {
+cudaError_t launch_gather(const void* x, const int32_t* pair_pos, int M, int top_k, int H,
+                          void* xs, int num_sms, cudaStream_t stream, bool pdl) {
   const int chunks = H / 8;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  // a warp per (row, 256-chunk segment)
-  cfg.gridDim = dim3(grid_for((long long)P * ((chunks + 255) / 256) * 32, 256, num_sms));
+  // a warp per (token, 256-chunk segment)
+  cfg.gridDim = dim3(grid_for((long long)M * ((chunks + 255) / 256) * 32, 256, num_sms));
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gather_kernel, reinterpret_cast<const uint4*>(x), sorted_pair,
-                            n_valid, top_k, chunks, reinterpret_cast<uint4*>(xs));
+  return cudaLaunchKernelEx(&cfg, gather_kernel, reinterpret_cast<const uint4*>(x), pair_pos, M,
+                            top_k, chunks, reinterpret_cast<uint4*>(xs));
 }
 
 cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int top_k, int E, int H,
@@ -240,7 +254,7 @@ cudaError_t launch_combine(const float* ypart, const int32_t* ids, int M, int to
 }
 
 cudaError_t launch_selftest_dequant(uint16_t* out, cudaStream_t stream) {
-  selftest_dequant_kernel<<<256, 32, 0, stream>>>(out);
+  selftest_dequant_kernel<<<256, 32, 0, stream>>>(out, dequant_mul());
   return cudaGetLastError();
 }
 
