@@ -96,6 +96,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct ForwardLayout {
   size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, route_scratch, xs, h, ypart, total;
+  size_t tile_order;  // split prefill schedule: the route's two-part tile order
   // decode schedule: arrival counters of FC1 and FC2 (cleared with the error word by one
   // memset: [0, clear_bytes)) and the partial accumulators of split units
   size_t sk_cnt1, sk_cnt2, clear_bytes, sk_part;
@@ -113,8 +114,9 @@ int check_shape(int M, int H, int I, int E, int top_k) {
 // The schedule a call runs.  PREFILL takes one of two tile shapes by the mean count
 // of pairs per expert: from 192 on, tiles of up to 320 pairs with one accumulator (an
 // expert's rows in one tile, the weights dequantized once per row block, the widest
-// MMAs); below, tiles of up to 192 pairs with two accumulators, so that the epilogue
-// of a tile overlaps the MMAs of the next (small tiles are epilogue-heavy).
+// MMAs); below, tiles of up to 192 pairs, those of more than 64 pairs on the prefill
+// kernel with two accumulators (the epilogue of a tile overlaps the MMAs of the next)
+// and the others on the decode kernel's weight-streaming pipeline.
 int resolve_sched(int sched, int M, int top_k, int E) {
   const long long P = (long long)M * top_k;
   if (sched == QMOE_SCHED_DECODE || sched == QMOE_SCHED_PREFILL_PAIR) return sched;
@@ -146,8 +148,11 @@ ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {
   off = align_up(off + 4 * (size_t)P, 256);
   L.tiles = off;
   off = align_up(off + 12 * (size_t)L.max_tiles, 256);
-  L.n_tiles = off;
-  off = align_up(off + 4, 256);
+  L.n_tiles = off;  // [2]: all tiles, tiles of the split order's first part
+  off = align_up(off + 8, 256);
+  L.tile_order = off;
+  if (resolve_sched(sched, M, top_k, E) == kSchedPrefillNarrow)
+    off = align_up(off + 4 * (size_t)L.max_tiles, 256);
   L.route_scratch = off;
   off = align_up(off + route_scratch_bytes(P, E), 1024);
   L.xs = off;
@@ -218,8 +223,10 @@ int qmoe_forward_kernel_count(int M, int top_k, int E, int sched) {
   if (sched < QMOE_SCHED_AUTO || sched > QMOE_SCHED_PREFILL_PAIR) return QMOE_ERR_ARG;
   if (M == 0) return 0;
   const long long P = (long long)M * top_k;
-  // the route (one kernel, or three above 8192 pairs), gather, FC1, FC2, combine
-  return 4 + (route_scratch_bytes(P, E) > 0 ? 3 : 1);
+  // the route (one kernel, or three above 8192 pairs), gather, FC1, FC2, combine; the
+  // split prefill schedule runs FC1 and FC2 as two launches each
+  const int split = resolve_sched(sched, M, top_k, E) == kSchedPrefillNarrow ? 2 : 0;
+  return 4 + split + (route_scratch_bytes(P, E) > 0 ? 3 : 1);
 }
 
 int qmoe_max_tiles(int M, int top_k, int E, int tile_n) {
@@ -325,9 +332,9 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   const int rsched = resolve_sched(sched, M, top_k, E);
   const int P = M * top_k;
   {
-    // the GEMMs count a CTA's K steps (decode: all units' steps) in 32 bits
-    const unsigned long long steps_cap = rsched == QMOE_SCHED_DECODE ? (1ull << 31)
-                                                                     : (unsigned long long)sms << 31;
+    // the GEMMs count a CTA's K steps (decode pipeline: all units' steps) in 32 bits
+    const bool all_steps = rsched == QMOE_SCHED_DECODE || rsched == kSchedPrefillNarrow;
+    const unsigned long long steps_cap = all_steps ? (1ull << 31) : (unsigned long long)sms << 31;
     const unsigned long long k1 = H / 128, k2 = I / 128;
     if ((unsigned long long)L.max_tiles * (2 * I / 128) * k1 >= steps_cap ||
         (unsigned long long)L.max_tiles * (H / 128) * k2 >= steps_cap)
@@ -349,6 +356,15 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   const int box_rows = gemm_b_box_rows(rsched), box_slabs = gemm_b_box_slabs(rsched);
   if (make_tmap_rows(&map_x, xs, L.rows, H, box_rows, box_slabs) != QMOE_OK) return QMOE_ERR_CUDA;
   if (make_tmap_rows(&map_h, h, L.rows, I, box_rows, box_slabs) != QMOE_OK) return QMOE_ERR_CUDA;
+  // split prefill schedule: the small tiles' launches read 3-D boxes of 64 rows
+  const bool split = rsched == kSchedPrefillNarrow;
+  int32_t* tile_order = split ? reinterpret_cast<int32_t*>(ws + L.tile_order) : nullptr;
+  CUtensorMap map_xs, map_hs;
+  if (split) {
+    const int br = gemm_b_box_rows(kSchedPrefillSmall), bs = gemm_b_box_slabs(kSchedPrefillSmall);
+    if (make_tmap_rows(&map_xs, xs, L.rows, H, br, bs) != QMOE_OK) return QMOE_ERR_CUDA;
+    if (make_tmap_rows(&map_hs, h, L.rows, I, br, bs) != QMOE_OK) return QMOE_ERR_CUDA;
+  }
 
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
@@ -356,7 +372,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   if (cudaMemsetAsync(err, 0, L.clear_bytes, s) != cudaSuccess) return QMOE_ERR_CUDA;
   if (!mark(0)) return QMOE_ERR_CUDA;
   cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
-                               n_tiles, err, ws + L.route_scratch, s);
+                               n_tiles, err, ws + L.route_scratch, s, tile_order, kSmallTileRows);
   if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
   const bool pdl = forward_uses_pdl(rsched);
   e = launch_gather(x_dev, pair_pos, M, top_k, H, xs, sms, s, pdl);
@@ -380,7 +396,13 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p1.dq_mul[2] = dequant_mul().m4;
   p1.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
   p1.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt1);
+  p1.tile_order = tile_order;
+  p1.tile_part = split ? 1 : 0;
   e = launch_gemm(GemmKind::kFc1, rsched, map_x, p1, sms, s);
+  if (e == cudaSuccess && split) {
+    p1.tile_part = 2;
+    e = launch_gemm(GemmKind::kFc1, kSchedPrefillSmall, map_xs, p1, sms, s);
+  }
   if (e != cudaSuccess || !mark(3)) return QMOE_ERR_CUDA;
 
   GemmParams p2;
@@ -402,7 +424,13 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p2.dq_mul[2] = dequant_mul().m4;
   p2.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
   p2.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt2);
+  p2.tile_order = tile_order;
+  p2.tile_part = split ? 1 : 0;
   e = launch_gemm(GemmKind::kFc2, rsched, map_h, p2, sms, s);
+  if (e == cudaSuccess && split) {
+    p2.tile_part = 2;
+    e = launch_gemm(GemmKind::kFc2, kSchedPrefillSmall, map_hs, p2, sms, s);
+  }
   if (e != cudaSuccess || !mark(4)) return QMOE_ERR_CUDA;
 
   e = launch_combine(ypart, topk_ids_dev, M, top_k, E, H, out_dev, sms, s, pdl);

@@ -200,6 +200,17 @@ __device__ __forceinline__ bool sk_reduce(const GemmParams& p, float (&v)[16], i
   return true;
 }
 
+// The units of a launch: each tile of its part (GemmParams::tile_part) times the p.nrb
+// weight row blocks, unit u = j * nrb + rb for the part's j-th tile.
+__device__ __forceinline__ int part_tiles(const GemmParams& p) {
+  if (p.tile_part == 0) return p.n_tiles[0];
+  return p.tile_part == 1 ? p.n_tiles[1] : p.n_tiles[0] - p.n_tiles[1];
+}
+__device__ __forceinline__ int part_tile(const GemmParams& p, int j) {
+  if (p.tile_part == 0) return j;
+  return p.tile_order[(p.tile_part == 1 ? 0 : p.n_tiles[1]) + j];
+}
+
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -218,6 +229,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   // MMA warps; otherwise 2-D boxes of kPairBoxRows rows from a producer warp
   constexpr int kWeightTmaWarp = weight_tma_warp(BIN);
   constexpr int kPairTmaWarp = pair_tma_warp(BIN);
+  // decode pipeline with tiles wider than 16 pairs: the warp after the MMA warps copies
+  // the pair rows (3-D boxes), so that the MMA warps' per-step work is one wait and the
+  // MMAs
+  constexpr bool PB = BIN && NMAX > 16;
+  constexpr int kPairBinWarp = kMmaWarp0 + NMW;
+  static_assert(!PB || kPairBinWarp < kEpiWarp0, "a free warp for the pair-row copies");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -251,7 +268,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       mbar_init(smem_u32(&rempty[s]), 4);
     }
     for (int s = 0; s < SL; ++s) {
-      for (int h = 0; h < KS; ++h) mbar_init(smem_u32(&sfull[s * KS + h]), h == 0 ? 5 : 4);
+      // the pair rows' copy counts on block 0's barrier, or with the producer warp (PB)
+      // on the last block's: there the MMA warp waits once per step, for every block
+      for (int h = 0; h < KS; ++h)
+        mbar_init(smem_u32(&sfull[s * KS + h]), h == (PB ? KS - 1 : 0) ? 5 : 4);
       mbar_init(smem_u32(&sempty[s]), 1);
     }
     for (int a = 0; a < ACCB; ++a) {
@@ -281,7 +301,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   const int nb128 = p.K / kBK;            // 128-wide weight blocks per unit
   const int nks = (nb128 + KS - 1) / KS;  // pipeline steps per unit
   const int last_halves = nb128 - (nks - 1) * KS;
-  const int n_units = (*p.n_tiles) * p.nrb;
+  const int n_units = part_tiles(p) * p.nrb;
   // BIN (decode, stream-K): the units' K steps form one sequence of n_units * nks steps,
   // cut into gridDim.x contiguous ranges, one per CTA; a unit split between CTAs is
   // summed from their partial accumulators in K order (sk_reduce).  Otherwise each CTA
@@ -289,7 +309,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   const unsigned long long n_steps = (unsigned long long)n_units * (unsigned long long)nks;
   uint32_t g0 = 0, total = 0;
   if constexpr (BIN) {
-    if (sk_split(n_units, nks, gridDim.x)) {
+    // units are split only with tiles of one 16-column chunk (the partial buffer's width)
+    if (NMAX == 16 && sk_split(n_units, nks, gridDim.x)) {
       g0 = sk_range_start(n_steps, blockIdx.x, gridDim.x);
       total = sk_range_start(n_steps, blockIdx.x + 1, gridDim.x) - g0;
     } else {  // whole units: a contiguous run of them per CTA, no partial sums
@@ -313,8 +334,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     bool ok = true;
     // local step it: weights of step ks of unit u
     auto issue = [&](int u, int ks) -> bool {
-      const int t = u / p.nrb, rb = u - t * p.nrb;
-      const int e = p.tiles[3 * t];
+      const int j = u / p.nrb, rb = u - j * p.nrb;
+      const int e = p.tiles[3 * part_tile(p, j)];
       const size_t blk = ((size_t)e * p.nrb + rb) * (size_t)nb128;
       const int s = it % RS;
       if (!warp_wait(smem_u32(&rempty[s]), ((it / RS) & 1) ^ 1, abort_flag, p.err)) return false;
@@ -351,7 +372,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const int t = u / p.nrb;
+      const int t = part_tile(p, u / p.nrb);
       const int start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int nbox = (rows + kPairBoxRows - 1) / kPairBoxRows;
       const uint32_t tx = (uint32_t)nbox * (uint32_t)(kPairBoxRows * 128);  // one slab
@@ -381,6 +402,33 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       while (globaltimer_ns() - t0 < 2000000ull) {
       }
     }
+  } else if (PB && warp == kPairBinWarp) {
+    // ------------------------------------------------------------ pair-row producer (PB)
+    // step i's rows into slot i % SL once the MMAs of step i - SL completed
+    const uint32_t leader = elect_one();
+    const uint64_t bpol = l2_policy_evict_last();
+    grid_dep_wait();  // the pair rows are the previous kernel's output
+    bool ok = true;
+    for (uint32_t bg = 0; bg < total && ok; ++bg) {
+      const uint32_t g = g0 + bg;
+      const int u = (int)(g / (uint32_t)nks);
+      const int bks = (int)(g - (uint32_t)u * nks);
+      const int bstart = p.tiles[3 * part_tile(p, u / p.nrb) + 1];
+      const uint32_t sl = bg % SL;
+      if (!warp_wait(smem_u32(&sempty[sl]), ((bg / SL) & 1) ^ 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&sfull[sl * KS + KS - 1]);
+      mbar_arrive_expect_tx_if(leader, fb, (uint32_t)C::kBBytes);
+      tma_load_3d_if(leader, smem_u32(bring + sl * C::kBBytes), &tmap_b, 0, bstart, 2 * KS * bks, fb,
+                     bpol);
+    }
+    if (!ok) {  // the pair rows of the last slots may still be landing
+      const unsigned long long t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + NMW) {
     // ------------------------------------------------------------ MMA issuers
     // MMA warp m takes the global K steps g with g % NMW == m, into its own accumulator.
@@ -404,7 +452,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const uint32_t g = g0 + bg;
       const int u = (int)(g / (uint32_t)nks);
       const int bks = (int)(g - (uint32_t)u * nks);
-      const int bstart = p.tiles[3 * (u / p.nrb) + 1];
+      const int bstart = p.tiles[3 * part_tile(p, u / p.nrb) + 1];
       const uint32_t sl = bg % SL;
       if (!warp_wait(sempty_u + sl * 8, ((bg / SL) & 1) ^ 1, abort_flag, p.err)) return false;
       const uint32_t fb = sfull_u + sl * KS * 8;
@@ -414,7 +462,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       bg += NMW;
       return true;
     };
-    if constexpr (BIN) {
+    if constexpr (BIN && !PB) {
       grid_dep_wait();  // the pair rows are the previous kernel's output
       ok = issue_b();
     }
@@ -429,7 +477,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         k0 = (int)(g - (uint32_t)u * nks);
         len = min(nks - k0, (int)(total - it));
       }
-      const int t = u / p.nrb;
+      const int t = part_tile(p, u / p.nrb);
       const int rows = p.tiles[3 * t + 2];
       const int n16 = ((rows + 15) >> 4) << 4;
       const uint32_t idesc = idesc_bf16_f32(128, n16 < 256 ? n16 : 256);
@@ -448,7 +496,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         const uint32_t sit = it + (uint32_t)ks;
         const int sl = sit % SL;
         const uint32_t sph = (sit / SL) & 1;
-        if (!warp_wait(sfull_u + sl * KS * 8, sph, abort_flag, p.err)) {
+        // PB: the last block's barrier completes after every block of the step and its
+        // pair rows; otherwise block 0's (the pair rows and block 0)
+        if (!warp_wait(sfull_u + (sl * KS + (PB ? KS - 1 : 0)) * 8, sph, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -482,7 +532,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
                             ks != ks0 ? 1u : 0u);
         }
         if (KS == 2 && (k0 + ks != nks - 1 || last_halves == 2)) {
-          if (!warp_wait(sfull_u + (sl * KS + 1) * 8, sph, abort_flag, p.err)) {
+          if (!PB && !warp_wait(sfull_u + (sl * KS + 1) * 8, sph, abort_flag, p.err)) {
             ok = false;
             break;
           }
@@ -492,7 +542,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
                             C::kBSlab >> 4, idesc, 1u);
         }
         tc_commit_if(leader, sempty_u + sl * 8);
-        if constexpr (BIN) {
+        if constexpr (BIN && !PB) {
           if (!issue_b()) {
             ok = false;
             break;
@@ -507,7 +557,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // no MMA may still be running when TMEM is released
     tc_commit_if(leader, smem_u32(drain));
     drain_wait(smem_u32(drain), 0);
-    if (BIN && !ok) {  // the pair rows of the last slots may still be landing
+    if (BIN && !PB && !ok) {  // the pair rows of the last slots may still be landing
       const unsigned long long t0 = globaltimer_ns();
       while (globaltimer_ns() - t0 < 2000000ull) {
       }
@@ -592,7 +642,8 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
         k0 = (int)(g - (uint32_t)u * nks);
         len = min(nks - k0, (int)(total - it0));
       }
-      const int t = u / p.nrb, rb = u - t * p.nrb;
+      const int j = u / p.nrb, rb = u - j * p.nrb;
+      const int t = part_tile(p, j);
       const int e = p.tiles[3 * t], start = p.tiles[3 * t + 1], rows = p.tiles[3 * t + 2];
       const int ab = local % ACCB;
       const float gsc = p.gscale[e] * 128.0f;  // 2^7 undoes the dequant's 2^-7
@@ -607,28 +658,34 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       const uint32_t tbase =
           tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol0 + ab * NMW * NMAX;
       if constexpr (BIN) {
-        static_assert(!BIN || NMAX == 16, "the decode schedule's tiles are one 16-column chunk");
-        float v[16];
+        static_assert(!BIN || NMAX % 16 == 0, "16-column chunks");
+        const bool whole = k0 == 0 && len == nks;  // always, unless NMAX == 16
+        // the tile's 16-column chunks one after the other (decode: the only one)
+        for (int c = 0; c < NMAX / 16; ++c) {
+          if (c > 0 && 16 * c >= rows) break;
+          float v[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = 0.f;
-        // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this segment
-        // iff its first step (m - it0 % NMW) mod NMW lies inside the segment
-        for (int m = 0; m < NMW; ++m) {
-          if ((m - (int)(it0 % NMW) + NMW) % NMW >= len) continue;
-          uint32_t r[16];
-          tmem_ld_x16(tbase + m * NMAX, r);
-          tmem_wait_ld();
-          tmem_ld_ready(r);
+          for (int k = 0; k < 16; ++k) v[k] = 0.f;
+          // accumulators in the fixed order m = 0, 1, ..; warp m holds MMAs of this
+          // segment iff its first step (m - it0 % NMW) mod NMW lies inside the segment
+          for (int m = 0; m < NMW; ++m) {
+            if ((m - (int)(it0 % NMW) + NMW) % NMW >= len) continue;
+            uint32_t r[16];
+            tmem_ld_x16(tbase + m * NMAX + 16 * c, r);
+            tmem_wait_ld();
+            tmem_ld_ready(r);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] += __uint_as_float(r[c]);
+            for (int k = 0; k < 16; ++k) v[k] += __uint_as_float(r[k]);
+          }
+          if (c == NMAX / 16 - 1 || 16 * (c + 1) >= rows) {
+            // the accumulator may be refilled once every warp has read it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acce[ab]));
+          }
+          if (whole || (NMAX == 16 && sk_reduce(p, v, u, nks, n_steps, g0, lane, q)))
+            epilogue_chunk_small<FC1, CLAMP>(p, v, lane, q, rb, start, rows, 16 * c, gsc);
         }
-        // the accumulator may be refilled once every warp has read it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&acce[ab]));
-        const bool whole = k0 == 0 && len == nks;
-        if (whole || sk_reduce(p, v, u, nks, n_steps, g0, lane, q))
-          epilogue_chunk_small<FC1, CLAMP>(p, v, lane, q, rb, start, rows, 0, gsc);
         it0 += len;
         ++local;
         continue;
@@ -721,13 +778,19 @@ bool forward_uses_pdl(int sched) { return sched != QMOE_SCHED_PREFILL; }
 
 int gemm_tile_n(int sched) {
   if (sched == QMOE_SCHED_DECODE) return 16;
+  if (sched == kSchedPrefillSmall) return kSmallTileRows;
   if (sched == QMOE_SCHED_PREFILL_PAIR) return 256;
   return sched == kSchedPrefillNarrow ? 192 : 320;
 }
 
-int gemm_b_box_rows(int sched) { return sched == QMOE_SCHED_DECODE ? 16 : kPairBoxRows; }
+int gemm_b_box_rows(int sched) {
+  if (sched == QMOE_SCHED_DECODE) return 16;
+  return sched == kSchedPrefillSmall ? kSmallTileRows : kPairBoxRows;
+}
 
-int gemm_b_box_slabs(int sched) { return sched == QMOE_SCHED_DECODE ? 4 : 0; }
+int gemm_b_box_slabs(int sched) {
+  return sched == QMOE_SCHED_DECODE || sched == kSchedPrefillSmall ? 4 : 0;
+}
 
 // decode : tiles <= 16 pairs, steps of 2 weight blocks (256 of K), 9 steps in flight
 //          (162 KB), 3 slots, 3 MMA warps x 2 accumulator buffers, 3 dequant groups, pair
@@ -753,6 +816,14 @@ cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, con
     if (clamp) return run<16, 9, 3, 2, 3, 3, 2, true, true, true>(tmap_b, p, g, stream);
     return fc1 ? run<16, 9, 3, 2, 3, 3, 2, true, true>(tmap_b, p, g, stream)
                : run<16, 9, 3, 2, 3, 3, 2, true, false>(tmap_b, p, g, stream);
+  }
+  if (sched == kSchedPrefillSmall) {
+    // the decode pipeline with tiles of up to 64 pairs: one MMA warp, three A slots
+    // of 256 of K, 6 weight steps in flight, whole units per CTA
+    const int g = num_sms < kMaxSkCtas ? num_sms : kMaxSkCtas;
+    if (clamp) return run<64, 6, 3, 2, 3, 1, 2, true, true, true>(tmap_b, p, g, stream);
+    return fc1 ? run<64, 6, 3, 2, 3, 1, 2, true, true>(tmap_b, p, g, stream)
+               : run<64, 6, 3, 2, 3, 1, 2, true, false>(tmap_b, p, g, stream);
   }
   if (sched == QMOE_SCHED_PREFILL_PAIR && !clamp && p.nrb % 2 == 0 && num_sms >= 2)
     return launch_gemm2(kind, tmap_b, p, num_sms, stream);

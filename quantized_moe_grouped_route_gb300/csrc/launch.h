@@ -12,9 +12,12 @@ constexpr int kRouteThreads = 512;
 size_t route_smem_bytes(int E);
 // scratch: route_scratch_bytes(P, E) bytes of device memory (none below 8193 pairs)
 size_t route_scratch_bytes(long long P, int E);
+// order (optional, needs small_rows < tile_n): the tile indices with the tiles of more
+// than small_rows pairs first, then the others; n_tiles[1] = the count of the first part
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
-                         unsigned int* err, void* scratch, cudaStream_t stream);
+                         unsigned int* err, void* scratch, cudaStream_t stream,
+                         int32_t* order = nullptr, int small_rows = 0);
 
 // misc.cu
 // scale_layout: QMOE_SCALES_PLAIN, _SWIZZLED_128X4 or _PACKED_U32
@@ -55,6 +58,11 @@ struct GemmParams {
   float* sk_part;
   int* sk_cnt;
   uint32_t dq_mul[3];  // the dequant's multipliers 64, 8, 4 (dequant_mul), as runtime values
+  // which tiles the launch covers: 0 all, in tile order; with the split prefill
+  // schedule's order (tile_order, n_tiles[1] = tiles of its first part) 1 the first
+  // part (tiles of more than kSmallTileRows pairs), 2 the second
+  const int32_t* tile_order;
+  int tile_part;
 };
 
 // Largest grid of the decode schedule (its partial buffer has a slot pair per CTA).
@@ -80,9 +88,14 @@ inline cudaLaunchAttribute pdl_attribute() {
 enum class GemmKind { kFc1, kFc2 };
 cudaError_t launch_gemm(GemmKind kind, int sched, const CUtensorMap& tmap_b, const GemmParams& p,
                         int num_sms, cudaStream_t stream);
-// Internal schedule: PREFILL with tiles of up to 192 pairs and two accumulators
-// (chosen for PREFILL when experts average fewer than 192 pairs).
+// Internal schedules.  kSchedPrefillNarrow: PREFILL when experts average fewer than 192
+// pairs; the route cuts tiles of up to 192 pairs and orders them into two parts, and
+// each GEMM runs as two launches: the tiles of more than kSmallTileRows pairs on the
+// prefill kernel (two accumulators), the others on kSchedPrefillSmall, the decode
+// kernel's weight-streaming pipeline with tiles of up to 64 pairs.
 constexpr int kSchedPrefillNarrow = 16;
+constexpr int kSchedPrefillSmall = 17;
+constexpr int kSmallTileRows = 64;
 int gemm_tile_n(int sched);  // max pairs per tile for a schedule
 // Prefill GEMM on CTA pairs (two SMs per M = 256 tile, gemm2.cu); needs an even number
 // of 128-row weight blocks (p.nrb).

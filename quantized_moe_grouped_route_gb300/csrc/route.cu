@@ -90,13 +90,17 @@ __device__ __forceinline__ bool warp_histogram(const int32_t* __restrict__ ids, 
 // B. From the R per-warp rows h[R][E] of counts (rows in pair order): offsets, the tile
 // list, and each row turned into that warp's first position per expert.  Thread t owns
 // experts [t*ept, (t+1)*ept).  Whole block; h in shared or global memory.
+// With `order` (the forward's split prefill schedule) it also lists the tile indices
+// with the tiles of more than `small_rows` pairs first and the others after them, each
+// part in tile order, and stores the count of the first part in n_tiles[1].
 __device__ __forceinline__ void route_scan(int* h, int R, int E, int T, int32_t* __restrict__ offsets,
                                            int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
-                                           int* scan_scratch) {
+                                           int* scan_scratch, int32_t* __restrict__ order = nullptr,
+                                           int small_rows = 0) {
   const int tid = threadIdx.x;
   const int ept = (E + kRouteThreads - 1) / kRouteThreads;
   const int e0 = tid * ept;
-  int my_pairs = 0, my_tiles = 0;
+  int my_pairs = 0, my_tiles = 0, my_small = 0;
   for (int j = 0; j < ept; ++j) {
     const int e = e0 + j;
     if (e < E) {
@@ -104,11 +108,19 @@ __device__ __forceinline__ void route_scan(int* h, int R, int E, int T, int32_t*
       for (int r = 0; r < R; ++r) c += h[(size_t)r * E + e];
       my_pairs += c;
       my_tiles += (c + T - 1) / T;
+      // every tile of an expert holds T pairs but the last, which holds c - T (n - 1)
+      if (c > 0 && c - T * ((c - 1) / T) <= small_rows) ++my_small;
     }
   }
   int total_pairs, total_tiles;
   int pair_base = block_exclusive_scan(my_pairs, scan_scratch, &total_pairs);
   int tile_base = block_exclusive_scan(my_tiles, scan_scratch, &total_tiles);
+  int wide_base = 0, small_base = 0, total_small = 0;
+  if (order) {
+    small_base = block_exclusive_scan(my_small, scan_scratch, &total_small);
+    wide_base = tile_base - small_base;  // wide tiles of the experts before this thread's
+  }
+  const int total_wide = total_tiles - total_small;
   for (int j = 0; j < ept; ++j) {
     const int e = e0 + j;
     if (e >= E) break;
@@ -121,16 +133,24 @@ __device__ __forceinline__ void route_scan(int* h, int R, int E, int T, int32_t*
     }
     const int cnt = run - pair_base;
     for (int s = 0; s < cnt; s += T) {
+      const int rows = min(T, cnt - s);
       tiles[3 * tile_base + 0] = e;
       tiles[3 * tile_base + 1] = pair_base + s;
-      tiles[3 * tile_base + 2] = min(T, cnt - s);
+      tiles[3 * tile_base + 2] = rows;
+      if (order) {
+        if (rows <= small_rows)
+          order[total_wide + small_base++] = tile_base;
+        else
+          order[wide_base++] = tile_base;
+      }
       ++tile_base;
     }
     pair_base = run;
   }
   if (tid == 0) {
     offsets[E] = total_pairs;
-    *n_tiles = total_tiles;
+    n_tiles[0] = total_tiles;
+    if (order) n_tiles[1] = total_wide;
   }
 }
 
@@ -181,7 +201,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const int32_t* __restrict__ ids, int P, int E, int T, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_pos,
                  int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
-                 unsigned int* __restrict__ err) {
+                 unsigned int* __restrict__ err, int32_t* __restrict__ order, int small_rows) {
   extern __shared__ int hist[];  // [kWarps][E]
   __shared__ int scan_scratch[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -193,7 +213,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   int* hw = hist + w * E;
   if (warp_histogram(ids, lo, hi, E, hw, lane)) atomicOr(err, QMOE_FLAG_BAD_ID);
   __syncthreads();
-  route_scan(hist, kWarps, E, T, offsets, tiles, n_tiles, scan_scratch);
+  route_scan(hist, kWarps, E, T, offsets, tiles, n_tiles, scan_scratch, order, small_rows);
   __syncthreads();
   warp_scatter(ids, lo, hi, E, hw, lane, sorted_pair, pair_pos);
   for (int pos = offsets[E] + tid; pos < P; pos += kRouteThreads) sorted_pair[pos] = -1;
@@ -219,9 +239,10 @@ __global__ void __launch_bounds__(kRouteThreads)
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_scan_kernel(int R, int E, int T, int* __restrict__ gh, int32_t* __restrict__ offsets,
-                      int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+                      int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
+                      int32_t* __restrict__ order, int small_rows) {
   __shared__ int scan_scratch[kWarps];
-  route_scan(gh, R, E, T, offsets, tiles, n_tiles, scan_scratch);
+  route_scan(gh, R, E, T, offsets, tiles, n_tiles, scan_scratch, order, small_rows);
 }
 
 __global__ void __launch_bounds__(kRouteThreads)
@@ -261,7 +282,8 @@ size_t route_scratch_bytes(long long P, int E) {
 
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
-                         unsigned int* err, void* scratch, cudaStream_t stream) {
+                         unsigned int* err, void* scratch, cudaStream_t stream, int32_t* order,
+                         int small_rows) {
   const size_t smem = route_smem_bytes(E);
   const int blocks = route_blocks(P);
   if (blocks == 1) {
@@ -269,7 +291,8 @@ cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* 
                                           (int)smem);
     if (rc != cudaSuccess) return rc;
     route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, P, E, tile_n, offsets, sorted_pair,
-                                                     pair_pos, tiles, n_tiles, err);
+                                                     pair_pos, tiles, n_tiles, err, order,
+                                                     small_rows);
     return cudaGetLastError();
   }
   int* gh = reinterpret_cast<int*>(scratch);
@@ -281,7 +304,7 @@ cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* 
   if (rc != cudaSuccess) return rc;
   route_hist_kernel<<<blocks, kRouteThreads, smem, stream>>>(ids, P, E, gh, err);
   route_scan_kernel<<<1, kRouteThreads, 0, stream>>>(blocks * kWarps, E, tile_n, gh, offsets, tiles,
-                                                     n_tiles);
+                                                     n_tiles, order, small_rows);
   route_scatter_kernel<<<blocks, kRouteThreads, smem, stream>>>(ids, P, E, gh, offsets, sorted_pair,
                                                                 pair_pos);
   return cudaGetLastError();

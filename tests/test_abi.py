@@ -38,6 +38,10 @@ def test_size_queries(lib):
     # kernels per forward: route (one, or three above 8192 pairs), gather, FC1, FC2, combine
     assert qmoe.qmoe_forward_kernel_count(16, 8, 256, qmoe.QMOE_SCHED_AUTO) == 5
     assert qmoe.qmoe_forward_kernel_count(8192, 8, 256, qmoe.QMOE_SCHED_AUTO) == 7
+    # experts averaging fewer than 192 pairs: FC1 and FC2 as two launches each (tiles of
+    # more than 64 pairs, then the others)
+    assert qmoe.qmoe_forward_kernel_count(2048, 8, 128, qmoe.QMOE_SCHED_AUTO) == 9
+    assert qmoe.qmoe_forward_kernel_count(512, 8, 128, qmoe.QMOE_SCHED_AUTO) == 7
     assert qmoe.qmoe_forward_kernel_count(0, 8, 256, qmoe.QMOE_SCHED_AUTO) == 0
     assert qmoe.qmoe_forward_kernel_count(4, 0, 8, qmoe.QMOE_SCHED_AUTO) == qmoe.QMOE_ERR_ARG
     assert qmoe.qmoe_repacked_fp4_size(256, 4096, 7168) == 256 * 4096 * 3584

@@ -61,7 +61,7 @@ def segments(g0, total, nks):
     return out
 
 
-def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None, g0=0):
+def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None, g0=0, PB=False):
     """One CTA running n_units units of nb128 weight blocks each (BIN: the global steps
     [g0, g0 + n_units * nks) of the stream-K sequence, which may start and end inside
     a unit).  Returns normally or raises ProtocolError (unsafe access) / RuntimeError
@@ -73,7 +73,10 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
     segs = segments(g0, total, nks) if BIN else [(u, 0, nks) for u in range(n_units)]
     rfull = [Bar(1) for _ in range(RS)]
     rempty = [Bar(4) for _ in range(RS)]
-    sfull = [Bar(5 if h == 0 else 4) for _ in range(SL) for h in range(KS)]
+    # PB: the decode pipeline with a pair-row producer warp; the copy counts on the step's
+    # last block barrier, and the MMA warps wait on that one alone
+    lastb = KS - 1 if PB else 0
+    sfull = [Bar(5 if h == lastb else 4) for _ in range(SL) for h in range(KS)]
     sempty = [Bar(1) for _ in range(SL)]
     bempty0 = [Bar(1) for _ in range(SL)]
     bfull1 = [Bar(1) for _ in range(SL)]
@@ -129,6 +132,22 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
                 later(fb, land)
                 yield True
 
+    def pair_producer_bin():  # PB: the producer warp, up to SL steps ahead
+        for bg in range(total):
+            sl = bg % SL
+            while plant != "no_b_wait" and not sempty[sl].done(((bg // SL) & 1) ^ 1):
+                yield False
+            check(bg < SL or read_done[sl][0] >= bg - SL,
+                  f"pair rows of slot {sl} refilled for step {bg} too early")
+            fb = sfull[sl * KS + lastb]
+            fb.expect_tx()
+            fb.arrive()
+
+            def land(sl=sl, g=bg):
+                b_slab[sl][0] = b_slab[sl][1] = g
+            later(fb, land)
+            yield True
+
     def mma_warp(m):
         bg = m  # BIN: next step whose pair rows this warp copies
 
@@ -137,7 +156,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
             if bg >= total:
                 return
             sl = bg % SL
-            while not sempty[sl].done(((bg // SL) & 1) ^ 1):
+            while plant != "no_b_wait" and not sempty[sl].done(((bg // SL) & 1) ^ 1):
                 yield False
             check(bg < SL or read_done[sl][0] >= bg - SL,
                   f"pair rows of slot {sl} refilled for step {bg} too early")
@@ -150,7 +169,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
             later(fb, land)
             bg += NMW
 
-        if BIN:
+        if BIN and not PB:
             yield from issue_b()
         it = 0
         for local, (_, k0, seg_len) in enumerate(segs):
@@ -163,7 +182,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
             for ks in range(ks0, seg_len, NMW):
                 sit = it + ks
                 sl, sph = sit % SL, (sit // SL) & 1
-                while not sfull[sl * KS].done(sph):
+                while not sfull[sl * KS + lastb].done(sph):
                     yield False
                 check(all(v == sit for v in a_slot[sl][0]), f"A slot {sl} not written for step {sit}")
                 check(b_slab[sl][0] == sit, f"pair rows of slot {sl} not landed for step {sit}")
@@ -176,7 +195,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
                             yield False
                     check(b_slab[sl][1] == sit, f"slab {sl}.1 not landed for step {sit}")
                 if KS == 2 and (k0 + ks != nks - 1 or last_halves == 2):
-                    while not sfull[sl * KS + 1].done(sph):
+                    while not PB and not sfull[sl * KS + 1].done(sph):
                         yield False
                     check(all(v == sit for v in a_slot[sl][1]),
                           f"A slot {sl} block 1 not written for step {sit}")
@@ -185,7 +204,7 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
                     read_done[sl][0] = max(read_done[sl][0], sit)
                     read_done[sl][1] = sit
                 later(sempty[sl], done)
-                if BIN:
+                if BIN and not PB:
                     yield from issue_b()
                 yield True
             it += seg_len
@@ -229,6 +248,8 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
     roles = [weight_producer()]
     if not BIN:
         roles.append(pair_producer())
+    elif PB:
+        roles.append(pair_producer_bin())
     roles += [mma_warp(m) for m in range(NMW)]
     roles += [dequant_warp(g, q) for g in range(DG) for q in range(4)]
     roles += [epilogue_warp(q) for q in range(4)]
@@ -259,10 +280,15 @@ def simulate(*, NMW, SL, RS, DG, ACCB, KS, BIN, nb128, n_units, seed, plant=None
 DECODE = dict(NMW=3, SL=3, RS=9, DG=3, ACCB=2, KS=2, BIN=True)
 PREFILL_WIDE = dict(NMW=1, SL=2, RS=6, DG=2, ACCB=1, KS=1, BIN=False)
 PREFILL_NARROW = dict(NMW=1, SL=2, RS=8, DG=2, ACCB=2, KS=1, BIN=False)
+# the split prefill schedule's small tiles: the decode pipeline with one MMA warp
+PREFILL_SMALL = dict(NMW=2, SL=2, RS=8, DG=2, ACCB=2, KS=2, BIN=True, PB=True)
+PREFILL_SMALL_1MMA = dict(NMW=1, SL=3, RS=6, DG=3, ACCB=2, KS=2, BIN=True, PB=True)
 
 
-@pytest.mark.parametrize("cfg", [DECODE, PREFILL_WIDE, PREFILL_NARROW],
-                         ids=["decode", "prefill_wide", "prefill_narrow"])
+@pytest.mark.parametrize("cfg", [DECODE, PREFILL_WIDE, PREFILL_NARROW, PREFILL_SMALL,
+                                 PREFILL_SMALL_1MMA],
+                         ids=["decode", "prefill_wide", "prefill_narrow", "prefill_small",
+                              "prefill_small_1mma"])
 @pytest.mark.parametrize("nb128", [1, 2, 3, 7, 16])
 def test_protocol_is_safe_and_live(cfg, nb128):
     for seed in range(12):
@@ -355,7 +381,10 @@ def test_stream_k_partition_and_reduction(n_units, nks, G):
 
 @pytest.mark.parametrize("plant,cfg", [("slab1_on_bempty0", PREFILL_WIDE),
                                        ("no_bfull1_wait", PREFILL_NARROW),
-                                       ("no_sempty_wait", DECODE)])
+                                       ("no_sempty_wait", DECODE),
+                                       ("no_sempty_wait", PREFILL_SMALL),
+                                       ("no_b_wait", PREFILL_SMALL),
+                                       ("no_b_wait", DECODE)])
 def test_planted_protocol_mistakes_are_caught(plant, cfg):
     with pytest.raises((ProtocolError, RuntimeError)):
         for seed in range(30):

@@ -52,6 +52,35 @@ def test_small_shapes_all_tokens(shape, sched):
     check_layer(li, out, layer._ws, sched, what=f"{name} sched={sched}")
 
 
+# Expert loads around the split prefill schedule's boundaries: tiles of up to 192 pairs,
+# those of at most 64 pairs on the decode pipeline, the rest on the prefill kernel.
+SPLIT_LOADS = [0, 1, 15, 16, 17, 63, 64, 65, 100, 128, 191, 192, 193, 256, 257, 300]
+
+
+@pytest.mark.parametrize("H,I", [(256, 128), (384, 384)])
+def test_split_prefill_tile_sizes(H, I):
+    """Every expert load of SPLIT_LOADS in one layer (1858 pairs over 16 experts, so the
+    prefill schedule splits its tiles): both parts of the tile order are non-empty and
+    every tile size at the boundaries occurs; with I = 384 FC2's last K step holds one
+    of its two 128-wide blocks."""
+    E, k = len(SPLIT_LOADS), 2
+    flat = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(SPLIT_LOADS)])
+    g = torch.Generator().manual_seed(23)
+    flat = flat[torch.randperm(flat.numel(), generator=g)]
+    M = flat.numel() // k
+    cfg = LayerConfig(f"split_h{H}_i{I}", M, H, I, E, k, seed=29)
+    li = make_inputs(cfg, "cpu")
+    li.topk_ids = flat[: M * k].view(M, k).contiguous()
+    li = li.to("cuda")
+    # route (one block), gather, two FC1 and two FC2 launches, combine
+    assert qmoe.qmoe_forward_kernel_count(M, k, E, qmoe.QMOE_SCHED_PREFILL) == 7
+    for sched in (qmoe.QMOE_SCHED_AUTO, qmoe.QMOE_SCHED_PREFILL):
+        out, layer = gpu_forward(li, sched)
+        check_layer(li, out, layer._ws, sched, what=f"split H={H} I={I} sched={sched}")
+        again, _ = gpu_forward(li, sched, layer=layer)
+        assert torch.equal(out, again), "the split schedule must be deterministic"
+
+
 def test_duplicate_experts_and_bad_ids():
     cfg = LayerConfig("dup", 24, 256, 128, 4, 3, seed=5)
     li = make_inputs(cfg, "cpu").to("cuda")
