@@ -593,32 +593,47 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
       if (!warp_wait(smem_u32(&sempty[a]), aph ^ 1, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * C::kSlotCols;
+      // the row's block scales of every block of the step as bf16x2 multipliers, looked
+      // up before the first TMEM store (whose ordering constraint would otherwise
+      // serialize the lookups behind the stores)
+      uint32_t sv[KS][8];
 #pragma unroll
       for (int h = 0; h < KS; ++h) {
         if (h < nh) {
-          // the row's 8 block scales as bf16x2 multipliers, looked up before the first
-          // TMEM store of the block (whose ordering constraint would otherwise
-          // serialize the lookups)
-          uint32_t sv[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            sv[j] = scale_lut[((j < 4 ? sc[h].x : sc[h].y) >> (8 * (j & 3))) & 0xFF];
+            sv[h][j] = scale_lut[((j < 4 ? sc[h].x : sc[h].y) >> (8 * (j & 3))) & 0xFF];
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < KS; ++h) {
+        if (h < nh) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint32_t o[16];
-            dequant8(cw[h][kk].x, sv[2 * kk], o + 0, dqm);
-            dequant8(cw[h][kk].y, sv[2 * kk], o + 4, dqm);
-            dequant8(cw[h][kk].z, sv[2 * kk + 1], o + 8, dqm);
-            dequant8(cw[h][kk].w, sv[2 * kk + 1], o + 12, dqm);
+            dequant8(cw[h][kk].x, sv[h][2 * kk], o + 0, dqm);
+            dequant8(cw[h][kk].y, sv[h][2 * kk], o + 4, dqm);
+            dequant8(cw[h][kk].z, sv[h][2 * kk + 1], o + 8, dqm);
+            dequant8(cw[h][kk].w, sv[h][2 * kk + 1], o + 12, dqm);
             tmem_st_x16(ta + h * 64 + kk * 16, o);
           }
-          tmem_wait_st();
-          tc_fence_before();
         }
-        // a block past the unit's end is left unwritten, but its barrier still
-        // completes so that every slot barrier advances once per use
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sfull[a * KS + h]));
+        // PB: the MMA warp waits for the last block only, so one wait for the stores
+        // serves all blocks; otherwise each block is published as soon as it is stored
+        // (the MMAs of block 0 start while block 1 is converted)
+        if (!PB || h == KS - 1) {
+          if (PB || h < nh) {
+            tmem_wait_st();
+            tc_fence_before();
+          }
+          // a block past the unit's end is left unwritten, but its barrier still
+          // completes so that every slot barrier advances once per use
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int b = PB ? 0 : h; b <= h; ++b) mbar_arrive(smem_u32(&sfull[a * KS + b]));
+          }
+        }
       }
       s += DG;
       if (s >= (uint32_t)RS) { s -= RS; rph ^= 1; }
