@@ -156,22 +156,35 @@ __device__ __forceinline__ bool sk_reduce(const GemmParams& p, float (&v)[16], i
                                           int q) {
   const unsigned int G = gridDim.x;
   const int row = q * 32 + lane;
-  const int slot = (int)(g0 / (uint32_t)nks) == u ? 0 : 1;
-  float4* mine = reinterpret_cast<float4*>(p.sk_part + ((size_t)(blockIdx.x * 2 + slot) * 128 + row) * 16);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) mine[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-  __threadfence();
-  __syncwarp();
   const unsigned long long first = (unsigned long long)u * nks, last = first + nks - 1;
   const unsigned int c0 = sk_cta_of(first, n_steps, G), c1 = sk_cta_of(last, n_steps, G);
   int nseg = 0;
   for (unsigned int c = c0; c <= c1; ++c)
     nseg += sk_range_start(n_steps, c + 1, G) > sk_range_start(n_steps, c, G);
-  int old = 0;
-  if (lane == 0) old = atomicAdd(p.sk_cnt + (size_t)u * 4 + q, 1);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != nseg - 1) return false;
-  __threadfence();
+  int* cnt = p.sk_cnt + (size_t)u * 4 + q;
+  // Every other segment already counted (the usual case for a CTA's last segment, whose
+  // unit the next CTA began at its start): this warp is the last one, and no other warp
+  // can see that count without having counted itself first.  Its own partial then needs
+  // no store, fence or count; each lane's acquire load orders its reads of the others'
+  // partials after their stores.
+  int seen;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(cnt) : "memory");
+  if (__all_sync(0xffffffffu, seen == nseg - 1)) {
+    // (falls through to the sum below)
+  } else {
+    const int slot = (int)(g0 / (uint32_t)nks) == u ? 0 : 1;
+    float4* mine =
+        reinterpret_cast<float4*>(p.sk_part + ((size_t)(blockIdx.x * 2 + slot) * 128 + row) * 16);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) mine[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    __threadfence();
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) old = atomicAdd(cnt, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != nseg - 1) return false;
+    __threadfence();
+  }
   float acc[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;
@@ -262,6 +275,9 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   uint8_t* epi_stage = ctrl + kCtrlBytes;                          // [4][NMAX] ids, weights
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the route's tile count, read before the set-up below so that its latency overlaps it
+  // (the route has completed before any GEMM of the forward starts)
+  const int n_part_tiles = part_tiles(p);
   if (threadIdx.x == 0) {
     for (int s = 0; s < RS; ++s) {
       mbar_init(smem_u32(&rfull[s]), 1);
@@ -301,7 +317,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   const int nb128 = p.K / kBK;            // 128-wide weight blocks per unit
   const int nks = (nb128 + KS - 1) / KS;  // pipeline steps per unit
   const int last_halves = nb128 - (nks - 1) * KS;
-  const int n_units = part_tiles(p) * p.nrb;
+  const int n_units = n_part_tiles * p.nrb;
   // BIN (decode, stream-K): the units' K steps form one sequence of n_units * nks steps,
   // cut into gridDim.x contiguous ranges, one per CTA; a unit split between CTAs is
   // summed from their partial accumulators in K order (sk_reduce).  Otherwise each CTA
