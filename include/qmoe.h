@@ -52,6 +52,9 @@ extern "C" {
 #define QMOE_SCHED_DECODE 1  /* tiles of <= 16 pairs: weight streaming, HBM bound */
 /* Tensor bound: tiles of <= 320 pairs when experts average >= 192 pairs, else tiles of
    <= 192 pairs whose epilogue overlaps the next tile's MMAs. */
+/* Prefill: tiles of up to 320 pairs; when experts average fewer than 192 pairs, tiles of
+   up to 192 pairs, with FC1 and FC2 each run as two launches (the tiles of more than 64
+   pairs, then the others on the decode pipeline). */
 #define QMOE_SCHED_PREFILL 2
 /* As PREFILL, with each 256-row weight tile on a pair of SMs (tcgen05 2-CTA MMAs, each
    SM holding half of the tile's pair rows); a GEMM whose count of 128-row weight blocks
@@ -157,7 +160,9 @@ int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E
  */
 size_t qmoe_forward_workspace_size(int M, int H, int I, int E, int top_k, int sched);
 /* Kernels one moe_nvfp4_forward call launches (route, gather, FC1, FC2, combine; the
- * route is three kernels above 8192 pairs); 0 for M = 0, QMOE_ERR_ARG for bad sizes. */
+ * route is three kernels above 8192 pairs, and FC1 and FC2 are two launches each on the
+ * prefill schedule when experts average fewer than 192 pairs); 0 for M = 0,
+ * QMOE_ERR_ARG for bad sizes. */
 int qmoe_forward_kernel_count(int M, int top_k, int E, int sched);
 int moe_nvfp4_forward(const void* x_dev, const uint8_t* w13_fp4_dev, const uint8_t* w13_scale_dev,
                       const float* w13_gscale_dev, const uint8_t* w2_fp4_dev,
