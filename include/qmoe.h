@@ -50,11 +50,10 @@ extern "C" {
 /* Tile schedules for moe_nvfp4_forward. */
 #define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
 #define QMOE_SCHED_DECODE 1  /* tiles of <= 16 pairs: weight streaming, HBM bound */
-/* Tensor bound: tiles of <= 320 pairs when experts average >= 192 pairs, else tiles of
-   <= 192 pairs whose epilogue overlaps the next tile's MMAs. */
-/* Prefill: tiles of up to 320 pairs; when experts average fewer than 192 pairs, tiles of
-   up to 192 pairs, with FC1 and FC2 each run as two launches (the tiles of more than 64
-   pairs, then the others on the decode pipeline). */
+/* Tensor bound: tiles of <= 320 pairs when experts average >= 192 pairs; else tiles of
+   <= 192 pairs, with FC1 and FC2 each run as two launches: the tiles of more than 64
+   pairs (whose epilogue overlaps the next tile's MMAs), then the others on the decode
+   pipeline. */
 #define QMOE_SCHED_PREFILL 2
 /* As PREFILL, with each 256-row weight tile on a pair of SMs (tcgen05 2-CTA MMAs, each
    SM holding half of the tile's pair rows); a GEMM whose count of 128-row weight blocks
