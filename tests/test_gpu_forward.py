@@ -57,14 +57,20 @@ def test_small_shapes_all_tokens(shape, sched):
 SPLIT_LOADS = [0, 1, 15, 16, 17, 63, 64, 65, 100, 128, 191, 192, 193, 256, 257, 300]
 
 
-@pytest.mark.parametrize("H,I", [(256, 128), (384, 384)])
-def test_split_prefill_tile_sizes(H, I):
+# Every expert between 65 and 192 pairs: the split schedule's second launch has no tiles.
+SPLIT_LOADS_WIDE = [65, 66, 80, 100, 127, 150, 191, 192, 70, 91]
+
+
+@pytest.mark.parametrize("H,I,loads", [(256, 128, SPLIT_LOADS), (384, 384, SPLIT_LOADS),
+                                       (256, 128, SPLIT_LOADS_WIDE)],
+                         ids=["h256_i128", "h384_i384", "h256_i128_all_wide"])
+def test_split_prefill_tile_sizes(H, I, loads):
     """Every expert load of SPLIT_LOADS in one layer (1858 pairs over 16 experts, so the
     prefill schedule splits its tiles): both parts of the tile order are non-empty and
     every tile size at the boundaries occurs; with I = 384 FC2's last K step holds one
-    of its two 128-wide blocks."""
-    E, k = len(SPLIT_LOADS), 2
-    flat = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(SPLIT_LOADS)])
+    of its two 128-wide blocks.  SPLIT_LOADS_WIDE leaves the second part empty."""
+    E, k = len(loads), 2
+    flat = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(loads)])
     g = torch.Generator().manual_seed(23)
     flat = flat[torch.randperm(flat.numel(), generator=g)]
     M = flat.numel() // k
