@@ -9,15 +9,18 @@
 // Each unit is one 128-row block of one expert's weights against one tile of that
 // expert's pairs (<= NMAX pairs) over the whole K: the weights are the MMA's M side
 // ("swap AB": weight rows on M = 128, pairs on N = 16..256; a wider tile as two
-// MMAs per K slice), so small per-expert
-// batches still fill the instruction, and every output element is produced by one
-// CTA in a fixed order (deterministic, no split reduction).
+// MMAs per K slice), so small per-expert batches still fill the instruction.  Every
+// output element is summed in a fixed order: by one CTA, or (decode pipeline, 16-pair
+// tiles) from the K-ordered partial sums of the CTAs a unit was split between
+// (sk_reduce), so results are deterministic.  A launch covers all tiles or one part
+// of the split prefill schedule's tile order (GemmParams::tile_part).
 //
 // Data path per pipeline step (KS x 128 of K):
 //   weight TMA    : bulk copies of the step's packed codes (8 KB per block) and scales
 //                   (1 KB per block) into the weight ring
 //   pair rows     : tiled TMA of the tile's gathered activations (bf16, 128-byte
-//                   swizzle) into the slot's shared-memory stage
+//                   swizzle) into the slot's shared-memory stage, from a producer warp
+//                   or (decode, 16-pair tiles) the MMA warps
 //   dequant warps : codes -> bf16 in registers (bit placement + one bf16x2 multiply
 //                   by the block scale) -> tcgen05.st into TMEM (the MMA's A operand)
 //   MMA warp(s)   : 8 x tcgen05.mma kind::f16 per block, A from TMEM, B from smem,
