@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -32,7 +33,9 @@ if ROOT not in sys.path:
 DEFAULT_CONFIG = "decode_m16_h7168_i2048_e256_k8"
 METRIC = "MoE layer tokens/s (decode M=16, H=7168, I=2048, E=256, top_k=8, NVFP4 W4A16)"
 STAGES = ["route", "gather", "fc1", "fc2", "combine"]
-KERNEL_SOURCES = ["csrc/gemm.cu", "csrc/dequant.cuh", "csrc/common.cuh", "csrc/epilogue.cuh"]
+# Files whose code decides the GEMMs' memory traffic: the kernels, the launch
+# configurations and schedules, the route's tile lists and the repacked layout.
+KERNEL_SOURCE_DIR = "csrc"
 
 
 def parse():
@@ -84,11 +87,26 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_source_sha():
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed: edits to comments
+    or layout leave the compiled kernels, and so the hash, unchanged."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_sha(root: str = None) -> str:
+    """Hash of the code (not the comments) of every source file that the profiled
+    kernels and their launches are built from."""
+    root = root or ROOT
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "quantized_moe_grouped_route_gb300", rel), "rb") as f:
-            h.update(f.read())
+    d = os.path.join(root, "quantized_moe_grouped_route_gb300", KERNEL_SOURCE_DIR)
+    files = [os.path.join(d, n) for n in sorted(os.listdir(d)) if n.endswith((".cu", ".cuh", ".h"))]
+    files.append(os.path.join(root, "include", "qmoe.h"))
+    for path in files:
+        with open(path) as f:
+            h.update(os.path.basename(path).encode())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
