@@ -172,7 +172,13 @@ def workspace_views(ws: torch.Tensor, M, H, I, E, top_k, sched=QMOE_SCHED_AUTO) 
         "pair_pos": view(L["pair_pos"], P, torch.int32),
         "tiles": view(L["tiles"], 3 * qmoe_max_tiles(M, top_k, E, qmoe_sched_tile_n(sched, M, top_k, E)),
                       torch.int32).view(-1, 3),
-        "n_tiles": view(L["n_tiles"], 1, torch.int32),
+        # [2]: all tiles and, on the split prefill schedule, its first part's count
+        "n_tiles": view(L["n_tiles"], 2, torch.int32),
+        # the split prefill schedule's two-part tile order: the 256-byte block after the
+        # counts (csrc/api.cu, forward_layout)
+        "tile_order": view(L["n_tiles"] + 256,
+                           qmoe_max_tiles(M, top_k, E, qmoe_sched_tile_n(sched, M, top_k, E)),
+                           torch.int32),
         "xs": view(L["xs"], rows * H, torch.bfloat16).view(rows, H),
         "h": view(L["h"], rows * I, torch.bfloat16).view(rows, I),
         "ypart": view(L["ypart"], P * H, torch.float32).view(P, H),

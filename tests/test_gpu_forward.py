@@ -87,6 +87,42 @@ def test_split_prefill_tile_sizes(H, I, loads):
         assert torch.equal(out, again), "the split schedule must be deterministic"
 
 
+def _tile_order_of(li, sched):
+    out, layer = gpu_forward(li, sched)
+    M, k = li.topk_ids.shape
+    c = li.cfg
+    v = qmoe.workspace_views(layer._ws, M, c.H, c.I, c.E, k, sched)
+    nt, nwide = (int(x) for x in v["n_tiles"].cpu())
+    return v["tiles"][:nt].cpu().numpy(), v["tile_order"][:nt].cpu().numpy(), nwide
+
+
+@pytest.mark.parametrize("case", ["mixed", "all_wide", "multi_block_route"])
+def test_split_tile_order(case):
+    """The route's two-part tile order on the split prefill schedule: the tiles of more
+    than 64 pairs first, then the others, each part in tile order, i.e. a stable
+    partition of the tile list (which the route tests check against the oracle); the
+    first part's count in n_tiles[1].  multi_block_route: above 8192 pairs, where the
+    order comes from the three-kernel route."""
+    if case == "multi_block_route":
+        # 8800 pairs over 64 experts, Zipf routing: heavy experts in several tiles, light ones
+        cfg = LayerConfig("split_mb", 1100, 128, 128, 64, 8, seed=31, routing="zipf")
+        li = make_inputs(cfg, "cpu").to("cuda")
+    else:
+        loads = SPLIT_LOADS if case == "mixed" else SPLIT_LOADS_WIDE
+        flat = torch.cat([torch.full((c,), e, dtype=torch.int32) for e, c in enumerate(loads)])
+        flat = flat[torch.randperm(flat.numel(), generator=torch.Generator().manual_seed(5))]
+        M = flat.numel() // 2
+        li = make_inputs(LayerConfig(f"order_{case}", M, 256, 128, len(loads), 2, seed=3), "cpu")
+        li.topk_ids = flat[: M * 2].view(M, 2).contiguous()
+        li = li.to("cuda")
+    tiles, order, nwide = _tile_order_of(li, qmoe.QMOE_SCHED_PREFILL)
+    wide = [t for t in range(len(tiles)) if tiles[t, 2] > 64]
+    small = [t for t in range(len(tiles)) if tiles[t, 2] <= 64]
+    assert nwide == len(wide)
+    assert order.tolist() == wide + small
+    assert len(small) > 0 or case == "all_wide"
+
+
 def test_duplicate_experts_and_bad_ids():
     cfg = LayerConfig("dup", 24, 256, 128, 4, 3, seed=5)
     li = make_inputs(cfg, "cpu").to("cuda")
