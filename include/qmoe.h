@@ -270,9 +270,11 @@ int qmoe_read_error(const void* workspace_dev, void* stream, uint32_t* flags_out
 
 /*
  * Diagnostics used by the tests (no counterpart on the pages).
- * qmoe_selftest_dequant: for every E2M1 code c (0..15) and E4M3 scale byte s
- *   (0..255) writes the kernel's dequantized bf16 of code*scale to
- *   out_dev[c * 256 + s] (uint16 bf16 bits, 4096 entries).  The product is exact.
+ * qmoe_selftest_dequant: dequantizes, for every c (0..15) and E4M3 scale byte s
+ *   (0..255), one packed word holding the E2M1 codes (c + j) mod 16 at its element
+ *   positions j = 0..7 with scale s, and writes the bf16 of code * scale of position j
+ *   to out_dev[(c * 256 + s) * 8 + j] (uint16 bf16 bits, 32768 entries, 64 KB).
+ *   Every product is exact.
  * qmoe_selftest_timeout: runs the bounded mbarrier wait of the GEMM kernels on a
  *   barrier nothing arrives at, with a limit of `limit_ns` nanoseconds, and records
  *   the expiry in the error word at workspace_dev (>= 256 bytes).  Returns

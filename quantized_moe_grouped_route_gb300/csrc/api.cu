@@ -392,8 +392,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p1.swiglu_limit = swiglu_limit;
   p1.err = err;
   p1.dq_mul[0] = dequant_mul().m64;
-  p1.dq_mul[1] = dequant_mul().m8;
-  p1.dq_mul[2] = dequant_mul().m4;
+  p1.dq_mul[1] = dequant_mul().m4;
   p1.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
   p1.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt1);
   p1.tile_order = tile_order;
@@ -420,8 +419,7 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   p2.H = H;
   p2.err = err;
   p2.dq_mul[0] = dequant_mul().m64;
-  p2.dq_mul[1] = dequant_mul().m8;
-  p2.dq_mul[2] = dequant_mul().m4;
+  p2.dq_mul[1] = dequant_mul().m4;
   p2.sk_part = reinterpret_cast<float*>(ws + L.sk_part);
   p2.sk_cnt = reinterpret_cast<int*>(ws + L.sk_cnt2);
   p2.tile_order = tile_order;

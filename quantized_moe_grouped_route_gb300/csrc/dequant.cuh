@@ -12,13 +12,18 @@
 // fp32 accumulator by 2^7 together with the global scale.
 //
 // The repack stores eight codes of one 32-bit word so that four output bf16x2 words
-// come out of shifts and masks with the mask M = 0x81C081C0 (magnitudes at bits
-// 6-8 / 22-24, signs at 15 / 31):
+// come out of shifts, one rotation and masks with the mask M = 0x81C081C0 (magnitudes
+// at bits 6-8 / 22-24, signs at 15 / 31):
 //   elements 0,1 : magnitude at bits  6- 8 / 22-24, sign 15 / 31   -> q & M
 //   elements 2,3 : magnitude at bits  0- 2 / 16-18, sign  9 / 25   -> (q << 6) & M
-//   elements 4,5 : magnitude at bits  3- 5 / 19-21, sign 12 / 28   -> (q << 3) & M
-//   elements 6,7 : magnitude bits 0,1 at 10,11 / 26,27, bit 2 at 14 / 30,
-//                  sign 13 / 29                                     -> three shifts
+//   elements 4,5 : magnitude at bits 26-28 / 10-12, sign  3 / 19   -> rotl(q, 12) & M
+//   elements 6,7 : magnitude bits 0,1 at 4,5 / 20,21, bit 2 at 14 / 30, sign 13 / 29
+//                  -> ((q << 2) & 0x80C080C0) | ((q >> 6) & 0x01000100)
+// Every bit of the word holds one bit of one code.  No packing gives each of the four
+// outputs one shift (or rotation) and one mask: the target bits {6, 7, 8, 15} of a half
+// tile no 32-bit word, so one output takes two pieces.  This one costs 13 instructions
+// per 8 codes (7 logic, 2 multiply-adds, 4 bf16x2 multiplies), against 15 for a
+// packing built from plain shifts alone.
 #pragma once
 
 #include <stdint.h>
@@ -39,16 +44,14 @@ __host__ __device__ __forceinline__ uint32_t pack_codes8(uint32_t plain) {
   q |= sgn(2) << 9;
   q |= mag(3) << 16;
   q |= sgn(3) << 25;
-  q |= mag(4) << 3;
-  q |= sgn(4) << 12;
-  q |= mag(5) << 19;
-  q |= sgn(5) << 28;
-  q |= (mag(6) & 1u) << 10;
-  q |= ((mag(6) >> 1) & 1u) << 11;
+  q |= mag(4) << 26;
+  q |= sgn(4) << 3;
+  q |= mag(5) << 10;
+  q |= sgn(5) << 19;
+  q |= (mag(6) & 3u) << 4;
   q |= ((mag(6) >> 2) & 1u) << 14;
   q |= sgn(6) << 13;
-  q |= (mag(7) & 1u) << 26;
-  q |= ((mag(7) >> 1) & 1u) << 27;
+  q |= (mag(7) & 3u) << 20;
   q |= ((mag(7) >> 2) & 1u) << 30;
   q |= sgn(7) << 29;
   return q;
@@ -62,15 +65,14 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 
 // Dequantize one packed word (eight consecutive K elements) with the broadcast
 // bf16x2 constant scale * 2^119; writes four bf16x2 words in K order.
-// The left shifts q * 2^k run as integer multiply-adds, on the multiply-add pipe: the
-// integer logic pipe, which the masks already keep busy, is the dequant's bound.  The
-// multipliers (64, 8, 4) are runtime values (DequantMul), so that the compiler keeps
-// them multiplies instead of turning them back into shifts (measured: 1% faster on the
-// decode schedule than compile-time constants).
+// The two left shifts q * 2^k run as integer multiply-adds, on the multiply-add pipe,
+// beside the logic ops on the integer pipe.  The multipliers (64, 4) are runtime
+// values (DequantMul), so that the compiler keeps them multiplies instead of turning
+// them back into shifts.
 struct DequantMul {
-  uint32_t m64, m8, m4;
+  uint32_t m64, m4;
 };
-__host__ __device__ constexpr DequantMul dequant_mul() { return DequantMul{64u, 8u, 4u}; }
+__host__ __device__ constexpr DequantMul dequant_mul() { return DequantMul{64u, 4u}; }
 
 __device__ __forceinline__ uint32_t shl_fma(uint32_t q, uint32_t pow2) {
   uint32_t r;
@@ -82,9 +84,8 @@ __device__ __forceinline__ void dequant8(uint32_t q, uint32_t s2, uint32_t* o, c
   const uint32_t M = 0x81C081C0u;
   const uint32_t a0 = q & M;
   const uint32_t a1 = shl_fma(q, m.m64) & M;
-  const uint32_t a2 = shl_fma(q, m.m8) & M;
-  const uint32_t a3 =
-      ((q >> 4) & 0x00C000C0u) | ((q >> 6) & 0x01000100u) | (shl_fma(q, m.m4) & 0x80008000u);
+  const uint32_t a2 = __funnelshift_l(q, q, 12) & M;  // rotate left by 12
+  const uint32_t a3 = (shl_fma(q, m.m4) & 0x80C080C0u) | ((q >> 6) & 0x01000100u);
   o[0] = bf16x2_mul(a0, s2);
   o[1] = bf16x2_mul(a1, s2);
   o[2] = bf16x2_mul(a2, s2);

@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
     // bits flip on each wrap.
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
     uint32_t pos = (g0 + (uint32_t)grp) % (uint32_t)nks;  // step of the current one within its unit
-    const DequantMul dqm{p.dq_mul[0], p.dq_mul[1], p.dq_mul[2]};
+    const DequantMul dqm{p.dq_mul[0], p.dq_mul[1]};
     for (uint32_t it = grp; it < total; it += DG) {
       const int nh = (KS == 2 && pos == (uint32_t)nks - 1) ? last_halves : KS;
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;

@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
     const int grp = (warp - kDequantWarp0) >> 2;
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const DequantMul dqm{p.dq_mul[0], p.dq_mul[1], p.dq_mul[2]};
+    const DequantMul dqm{p.dq_mul[0], p.dq_mul[1]};
     uint32_t s = grp, a = grp, rph = 0, aph = 0;
     for (uint32_t it = grp; it < total; it += DG) {
       if (!warp_wait(smem_u32(&rfull[s]), rph, abort_flag, p.err)) break;

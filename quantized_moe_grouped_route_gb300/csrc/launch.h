@@ -57,7 +57,7 @@ struct GemmParams {
   // quarter), zero at launch
   float* sk_part;
   int* sk_cnt;
-  uint32_t dq_mul[3];  // the dequant's multipliers 64, 8, 4 (dequant_mul), as runtime values
+  uint32_t dq_mul[2];  // the dequant's multipliers 64, 4 (dequant_mul), as runtime values
   // which tiles the launch covers: 0 all, in tile order; with the split prefill
   // schedule's order (tile_order, n_tiles[1] = tiles of its first part) 1 the first
   // part (tiles of more than kSmallTileRows pairs), 2 the second

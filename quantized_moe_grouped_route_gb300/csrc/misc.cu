@@ -165,23 +165,27 @@ __global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* _
   }
 }
 
-// Every (code, scale) pair through the GEMM's dequant path (with its multipliers passed
-// in at run time, as the GEMM gets them).
+// Every (code, scale) pair at every element position of a packed word, through the
+// GEMM's dequant path (with its multipliers passed in at run time, as the GEMM gets
+// them).  Thread c fills the word with codes (c + j) mod 16 at positions j = 0..7, so
+// each position meets all 16 codes beside 7 other nonzero codes.
 __global__ void selftest_dequant_kernel(uint16_t* __restrict__ out, DequantMul dqm) {
   const int sb = blockIdx.x;  // scale byte
   const int c = threadIdx.x;  // 0..15
   if (c >= 16) return;
   const uint32_t s2 = e4m3_scale_bf16x2(sb);
-  // put code c at element position (c % 8) of a word, zeros elsewhere
-  const int pos = c & 7;
-  const uint32_t plain = (uint32_t)c << (4 * pos);
+  uint32_t plain = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) plain |= (uint32_t)((c + j) & 15) << (4 * j);
   uint32_t o[4];
   dequant8(pack_codes8(plain), s2, o, dqm);
-  const uint32_t word = o[pos >> 1];
-  const uint16_t v = (pos & 1) ? (uint16_t)(word >> 16) : (uint16_t)(word & 0xFFFF);
-  // undo the 2^-7 the kernels fold into the epilogue: multiply by 128 exactly
-  const float f = __bfloat162float(__ushort_as_bfloat16(v)) * 128.0f;
-  out[c * 256 + sb] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint16_t v = (j & 1) ? (uint16_t)(o[j >> 1] >> 16) : (uint16_t)(o[j >> 1] & 0xFFFF);
+    // undo the 2^-7 the kernels fold into the epilogue: multiply by 128 exactly
+    const float f = __bfloat162float(__ushort_as_bfloat16(v)) * 128.0f;
+    out[((size_t)c * 256 + sb) * 8 + j] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  }
 }
 
 // One bounded wait on a barrier that nothing ever arrives at.

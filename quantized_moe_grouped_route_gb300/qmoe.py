@@ -335,7 +335,7 @@ def qmoe_noalloc_read_error(stream=None):
 
 
 def qmoe_selftest_dequant(device="cuda", stream=None) -> torch.Tensor:
-    out = torch.empty(16 * 256, dtype=torch.int16, device=device)
+    out = torch.empty(16 * 256 * 8, dtype=torch.int16, device=device)
     _check("qmoe_selftest_dequant", lib().qmoe_selftest_dequant(_ptr(out), _stream(stream)))
     return out
 

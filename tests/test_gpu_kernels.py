@@ -18,16 +18,20 @@ pytestmark = pytest.mark.gpu
 
 
 def test_dequant_every_code_and_scale():
-    """kernel dequant(code, scale) == E2M1(code) * E4M3(scale), all 16 x 256 pairs, exact."""
-    got = qmoe.qmoe_selftest_dequant().cpu().numpy().astype(np.uint16).reshape(16, 256)
+    """kernel dequant(code, scale) == E2M1(code) * E4M3(scale), all 16 x 256 pairs at
+    each of the 8 element positions of a packed word (the other positions holding other
+    codes), exact."""
+    got = qmoe.qmoe_selftest_dequant().cpu().numpy().astype(np.uint16).reshape(16, 256, 8)
     gotf = oracle.bf16_bits_to_float(got)
     for c in range(16):
-        for s in range(256):
-            want = oracle.dec_e2m1(c) * oracle.dec_e4m3(s)
-            if np.isnan(want):
-                assert np.isnan(gotf[c, s]), (c, s)
-            else:
-                assert gotf[c, s] == want, (c, s, gotf[c, s], want)
+        for j in range(8):
+            code = (c + j) % 16
+            for s in range(256):
+                want = oracle.dec_e2m1(code) * oracle.dec_e4m3(s)
+                if np.isnan(want):
+                    assert np.isnan(gotf[c, s, j]), (c, j, s)
+                else:
+                    assert gotf[c, s, j] == want, (c, j, s, gotf[c, s, j], want)
 
 
 def _unpack_repacked(codes: np.ndarray, scales: np.ndarray, E, N, K, w13: bool):
@@ -37,7 +41,7 @@ def _unpack_repacked(codes: np.ndarray, scales: np.ndarray, E, N, K, w13: bool):
     words = codes.view(np.uint32).reshape(E, nrb, nks, 4, 128, 4)
     # element j of a packed word -> (bit positions of magnitude bits 0,1,2 and sign)
     pos = {0: (6, 7, 8, 15), 1: (22, 23, 24, 31), 2: (0, 1, 2, 9), 3: (16, 17, 18, 25),
-           4: (3, 4, 5, 12), 5: (19, 20, 21, 28), 6: (10, 11, 14, 13), 7: (26, 27, 30, 29)}
+           4: (26, 27, 28, 3), 5: (10, 11, 12, 19), 6: (4, 5, 14, 13), 7: (20, 21, 30, 29)}
     plain = np.zeros((E, nrb, nks, 4, 128, 4, 8), np.uint8)
     for j, (b0, b1, b2, bs) in pos.items():
         v = (((words >> b0) & 1) | (((words >> b1) & 1) << 1) | (((words >> b2) & 1) << 2)
