@@ -35,7 +35,7 @@ constexpr int kCodeBytes = 8192;
 constexpr int kScaleBytes = 1024;
 constexpr int kRawBytes = kCodeBytes + kScaleBytes;
 constexpr int kTmemCols = 512;
-constexpr int kCtrlBytes = 2048;
+constexpr int kCtrlBytes = 1024;  // barriers, TMEM slot, abort flag
 constexpr int kNmax = 256;             // pairs per tile (both CTAs)
 constexpr int kHalfRows = kNmax / 2;   // pair rows per CTA
 constexpr int kBoxRows = 64;           // rows of a 2-D pair-row box
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
   uint64_t* drain = acce + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint32_t* scale_lut = reinterpret_cast<uint32_t*>(ctrl + 1024);
+  __shared__ uint32_t scale_lut[256];  // at a fixed shared address (cheaper lookups)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
