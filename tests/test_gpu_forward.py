@@ -36,6 +36,9 @@ SMALL = [
     # CTAs, most CTAs idle) and a few steps per CTA (units split over many CTAs)
     ("sk_m1_h1024_i1024_e4_k1", 1, 1024, 1024, 4, 1),
     ("sk_m3_h7168_i512_e2_k2", 3, 7168, 512, 2, 2),
+    # decode schedule with more than two FC1 units per CTA (about 500 units of 4 steps on
+    # 152 SMs), split: most CTAs start and end inside a unit
+    ("sk_m16_h1024_i2048_e16_k8", 16, 1024, 2048, 16, 8),
 ]
 
 
