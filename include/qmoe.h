@@ -46,6 +46,7 @@ extern "C" {
 /* Device error-word bits (qmoe_read_error). */
 #define QMOE_FLAG_BAD_ID 1u
 #define QMOE_FLAG_TIMEOUT 2u
+#define QMOE_FLAG_INTERNAL 4u /* a kernel's check of a hardware contract failed */
 
 /* Tile schedules for moe_nvfp4_forward. */
 #define QMOE_SCHED_AUTO 0    /* DECODE when M * top_k <= 4 * E, else PREFILL */
@@ -263,7 +264,8 @@ int moe_nvfp4_forward_events(const void* x_dev, const uint8_t* w13_fp4_dev,
 /*
  * qmoe_read_error — copy the device error word (first 4 bytes of a route or forward
  * workspace) to the host after the stream's work so far; synchronises `stream`.
- * *flags_out gets the QMOE_FLAG_* bits.  Returns QMOE_ERR_TIMEOUT if the timeout
+ * *flags_out gets the QMOE_FLAG_* bits.  Returns QMOE_ERR_CUDA if the internal bit
+ * is set (the layer's results are not valid), else QMOE_ERR_TIMEOUT if the timeout
  * bit is set, else QMOE_ERR_BAD_ID if the bad-id bit is set, else QMOE_OK.
  */
 int qmoe_read_error(const void* workspace_dev, void* stream, uint32_t* flags_out);

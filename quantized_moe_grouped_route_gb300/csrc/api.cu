@@ -524,6 +524,7 @@ int qmoe_read_error(const void* workspace_dev, void* stream, uint32_t* flags_out
       cudaStreamSynchronize(s) != cudaSuccess)
     return QMOE_ERR_CUDA;
   *flags_out = flags;
+  if (flags & QMOE_FLAG_INTERNAL) return QMOE_ERR_CUDA;
   if (flags & QMOE_FLAG_TIMEOUT) return QMOE_ERR_TIMEOUT;
   if (flags & QMOE_FLAG_BAD_ID) return QMOE_ERR_BAD_ID;
   return QMOE_OK;

@@ -95,8 +95,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 // One lane of a converged warp; used as a predicate so that the single-thread
 // instructions below (TMA, MMA, commit) are issued once while the warp's control
-// flow stays uniform (issuing them from a divergent single thread is several times
-// slower).
+// flow stays uniform (issuing the copies from a divergent single thread was several
+// times slower; the decode MMAs, whose operands the compiler can keep uniform, measured
+// fewer instructions inside the elected lane's branch).
 __device__ __forceinline__ uint32_t elect_one() {
   uint32_t pred;
   asm volatile(

@@ -318,7 +318,13 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // The CTA allocates all 512 TMEM columns, so the allocation can only start at lane 0,
+  // column 0: the base is the constant 0, which lets the compiler keep the TMEM operands
+  // of the MMAs uniform (measured with the MMA issue below: decode M=16 layer 479 -> 474
+  // µs).  The address the allocation wrote is still checked.
+  static_assert(kTmemCols == 512, "the constant TMEM base needs the whole TMEM");
+  const uint32_t tmem = 0u;
+  if (threadIdx.x == 0 && *tmem_slot != 0u && p.err) atomicOr(p.err, QMOE_FLAG_INTERNAL);
 
   const int nb128 = p.K / kBK;            // 128-wide weight blocks per unit
   const int nks = (nb128 + KS - 1) / KS;  // pipeline steps per unit
@@ -549,9 +555,12 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           else
             mma_bf16_ts_slab4(leader, d_tmem, a0 + 32, b1, bdesc_hi, idesc, 1u);
         } else {
-          mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols,
-                            bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4, idesc,
-                            ks != ks0 ? 1u : 0u);
+          // issued inside the elected lane's branch: fewer instructions than the
+          // predicated form here (measured: decode FC2 -2.5%)
+          if (leader)
+            mma_bf16_ts_step8(1u, d_tmem, tmem + sl * C::kSlotCols,
+                              bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4,
+                              idesc, ks != ks0 ? 1u : 0u);
         }
         if (KS == 2 && (k0 + ks != nks - 1 || last_halves == 2)) {
           if (!PB && !warp_wait(sfull_u + (sl * KS + 1) * 8, sph, abort_flag, p.err)) {
@@ -559,9 +568,10 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
             break;
           }
           tc_fence_after();
-          mma_bf16_ts_step8(leader, d_tmem, tmem + sl * C::kSlotCols + 64,
-                            bdesc_lo0 + ((sl * C::kBBytes + 2 * C::kBSlab) >> 4), bdesc_hi,
-                            C::kBSlab >> 4, idesc, 1u);
+          if (leader)
+            mma_bf16_ts_step8(1u, d_tmem, tmem + sl * C::kSlotCols + 64,
+                              bdesc_lo0 + ((sl * C::kBBytes + 2 * C::kBSlab) >> 4), bdesc_hi,
+                              C::kBSlab >> 4, idesc, 1u);
         }
         tc_commit_if(leader, sempty_u + sl * 8);
         if constexpr (BIN && !PB) {

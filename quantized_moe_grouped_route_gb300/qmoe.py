@@ -28,6 +28,7 @@ QMOE_ERR_WORKSPACE = -6
 QMOE_ERR_BAD_ID = -7
 QMOE_FLAG_BAD_ID = 1
 QMOE_FLAG_TIMEOUT = 2
+QMOE_FLAG_INTERNAL = 4
 QMOE_SCHED_AUTO = 0
 QMOE_SCHED_DECODE = 1
 QMOE_SCHED_PREFILL = 2

@@ -156,6 +156,17 @@ def test_timeout_is_reported_not_hung():
     assert float(x.sum()) == 4.0
 
 
+def test_error_word_bits_map_to_return_codes():
+    """qmoe_read_error: the internal-check bit wins over timeout, timeout over bad id."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for word, want in [(0, qmoe.QMOE_OK), (qmoe.QMOE_FLAG_BAD_ID, qmoe.QMOE_ERR_BAD_ID),
+                       (qmoe.QMOE_FLAG_TIMEOUT | qmoe.QMOE_FLAG_BAD_ID, qmoe.QMOE_ERR_TIMEOUT),
+                       (qmoe.QMOE_FLAG_INTERNAL | qmoe.QMOE_FLAG_TIMEOUT, qmoe.QMOE_ERR_CUDA)]:
+        ws[:4] = torch.tensor([word], dtype=torch.int32).view(torch.uint8).to("cuda")
+        rc, flags = qmoe.qmoe_read_error(ws)
+        assert (rc, flags) == (want, word)
+
+
 def test_argument_errors():
     x = torch.zeros(4, 100, dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros(4, 2, dtype=torch.int32, device="cuda")
