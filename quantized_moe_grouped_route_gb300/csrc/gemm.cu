@@ -537,11 +537,14 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           const uint32_t a0 = tmem + sl * C::kSlotCols;
           const uint32_t b0 = bdesc_lo0 + sl * (C::kBBytes >> 4);
           const uint32_t acc = ks != ks0 ? 1u : 0u;
-          if (NMAX > 256 && n16 > 256)
-            mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0, b0, bdesc_hi, (256 * 128) >> 4,
-                                idesc, idesc2, acc);
-          else
-            mma_bf16_ts_slab4(leader, d_tmem, a0, b0, bdesc_hi, idesc, acc);
+          // the MMAs are issued inside the elected lane's branch (see below)
+          if (leader) {
+            if (NMAX > 256 && n16 > 256)
+              mma_bf16_ts_slab4x2(1u, d_tmem, d_tmem + 256, a0, b0, bdesc_hi, (256 * 128) >> 4,
+                                  idesc, idesc2, acc);
+            else
+              mma_bf16_ts_slab4(1u, d_tmem, a0, b0, bdesc_hi, idesc, acc);
+          }
           tc_commit_if(leader, bempty0_u + sl * 8);
           if (!warp_wait(bfull1_u + sl * 8, sph, abort_flag, p.err)) {
             ok = false;
@@ -549,14 +552,17 @@ __global__ void __launch_bounds__(gemm_threads(DG), 1)
           }
           tc_fence_after();
           const uint32_t b1 = b0 + (C::kBSlab >> 4);
-          if (NMAX > 256 && n16 > 256)
-            mma_bf16_ts_slab4x2(leader, d_tmem, d_tmem + 256, a0 + 32, b1, bdesc_hi,
-                                (256 * 128) >> 4, idesc, idesc2, 1u);
-          else
-            mma_bf16_ts_slab4(leader, d_tmem, a0 + 32, b1, bdesc_hi, idesc, 1u);
+          if (leader) {
+            if (NMAX > 256 && n16 > 256)
+              mma_bf16_ts_slab4x2(1u, d_tmem, d_tmem + 256, a0 + 32, b1, bdesc_hi,
+                                  (256 * 128) >> 4, idesc, idesc2, 1u);
+            else
+              mma_bf16_ts_slab4(1u, d_tmem, a0 + 32, b1, bdesc_hi, idesc, 1u);
+          }
         } else {
-          // issued inside the elected lane's branch: fewer instructions than the
-          // predicated form here (measured: decode FC2 -2.5%)
+          // Issued inside the elected lane's branch rather than predicated per lane: with
+          // operands the compiler can keep uniform the MMA warp's issue takes about half
+          // the instructions (measured: decode FC2 -2.5%, skewed prefill FC1 -1%).
           if (leader)
             mma_bf16_ts_step8(1u, d_tmem, tmem + sl * C::kSlotCols,
                               bdesc_lo0 + sl * (C::kBBytes >> 4), bdesc_hi, C::kBSlab >> 4,

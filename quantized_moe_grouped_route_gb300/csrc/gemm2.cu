@@ -350,8 +350,10 @@ __global__ void __launch_bounds__(gemm2_threads(DG), 1)
           break;
         }
         tc_fence_after();
-        mma2_step8(lead, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (kBBytes >> 4), bdesc_hi,
-                   kBSlab >> 4, idesc, ks != 0 ? 1u : 0u);
+        // issued inside the elected lane's branch, as in the single-SM kernel
+        if (lead)
+          mma2_step8(1u, d_tmem, tmem + sl * 64, bdesc_lo0 + sl * (kBBytes >> 4), bdesc_hi,
+                     kBSlab >> 4, idesc, ks != 0 ? 1u : 0u);
         tc_commit2_both_if(lead, sempty_u + sl * 8);
       }
       if (ok) tc_commit2_both_if(lead, smem_u32(accf));
