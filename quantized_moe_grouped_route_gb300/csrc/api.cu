@@ -133,9 +133,9 @@ ForwardLayout forward_layout(int M, int H, int I, int E, int top_k, int sched) {
   const bool sk = resolve_sched(sched, M, top_k, E) == QMOE_SCHED_DECODE;
   size_t off = kWsHeaderBytes;
   L.sk_cnt1 = off;
-  off += sk ? sk_cnt_bytes((long long)L.max_tiles * (2 * I / 128)) : 0;
+  off += sk ? sk_cnt_bytes(kMaxSkCtas) : 0;
   L.sk_cnt2 = off;
-  off += sk ? sk_cnt_bytes((long long)L.max_tiles * (H / 128)) : 0;
+  off += sk ? sk_cnt_bytes(kMaxSkCtas) : 0;
   L.clear_bytes = off;
   off = align_up(off, 256);
   L.sk_part = off;
@@ -369,12 +369,18 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
   };
-  if (cudaMemsetAsync(err, 0, L.clear_bytes, s) != cudaSuccess) return QMOE_ERR_CUDA;
+  // the one-block route zeroes the error word and the split-unit counters itself (and
+  // runs as a programmatic dependent of the stream's previous kernel); before the
+  // multi-block route a memset does
+  const bool pdl = forward_uses_pdl(rsched);
+  const bool route_clears = route_blocks(P) == 1;
+  if (!route_clears && cudaMemsetAsync(err, 0, L.clear_bytes, s) != cudaSuccess)
+    return QMOE_ERR_CUDA;
   if (!mark(0)) return QMOE_ERR_CUDA;
   cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
-                               n_tiles, err, ws + L.route_scratch, s, tile_order, kSmallTileRows);
+                               n_tiles, err, ws + L.route_scratch, s, tile_order, kSmallTileRows,
+                               (int)(L.clear_bytes / 4), pdl && route_clears);
   if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
-  const bool pdl = forward_uses_pdl(rsched);
   e = launch_gather(x_dev, pair_pos, M, top_k, H, xs, sms, s, pdl);
   if (e != cudaSuccess || !mark(2)) return QMOE_ERR_CUDA;
 

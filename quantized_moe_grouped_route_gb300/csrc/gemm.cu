@@ -164,7 +164,9 @@ __device__ __forceinline__ bool sk_reduce(const GemmParams& p, float (&v)[16], i
   int nseg = 0;
   for (unsigned int c = c0; c <= c1; ++c)
     nseg += sk_range_start(n_steps, c + 1, G) > sk_range_start(n_steps, c, G);
-  int* cnt = p.sk_cnt + (size_t)u * 4 + q;
+  // one counter per (split unit, lane quarter), indexed by the CTA that holds the unit's
+  // first step: a CTA's range starts at most one unit that runs past its end
+  int* cnt = p.sk_cnt + (size_t)c0 * 4 + q;
   // Every other segment already counted (the usual case for a CTA's last segment, whose
   // unit the next CTA began at its start): this warp is the last one, and no other warp
   // can see that count without having counted itself first.  Its own partial then needs

@@ -14,10 +14,15 @@ size_t route_smem_bytes(int E);
 size_t route_scratch_bytes(long long P, int E);
 // order (optional, needs small_rows < tile_n): the tile indices with the tiles of more
 // than small_rows pairs first, then the others; n_tiles[1] = the count of the first part
+// With one block (route_blocks(P) == 1) the kernel first zeroes clear_words 32-bit words
+// from err on; with several the caller must have zeroed the error word.  pdl: launch the
+// one-block form with programmatic stream serialization.
+int route_blocks(long long P);
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
                          unsigned int* err, void* scratch, cudaStream_t stream,
-                         int32_t* order = nullptr, int small_rows = 0);
+                         int32_t* order = nullptr, int small_rows = 0, int clear_words = 1,
+                         bool pdl = false);
 
 // misc.cu
 // scale_layout: QMOE_SCALES_PLAIN, _SWIZZLED_128X4 or _PACKED_U32
@@ -53,8 +58,8 @@ struct GemmParams {
   int H;
   unsigned int* err;
   // decode schedule (stream-K): fp32 partial accumulators of units split between CTAs,
-  // [CTA][2 slots][128 rows][16 pairs], and one arrival counter per (unit, TMEM lane
-  // quarter), zero at launch
+  // [CTA][2 slots][128 rows][16 pairs], and one arrival counter per (split unit, TMEM
+  // lane quarter), [CTA holding the unit's first step][4], zero at launch
   float* sk_part;
   int* sk_cnt;
   uint32_t dq_mul[2];  // the dequant's multipliers 64, 4 (dequant_mul), as runtime values
@@ -69,7 +74,7 @@ struct GemmParams {
 constexpr int kMaxSkCtas = 192;
 // Bytes of the decode schedule's partial buffer and of its counters for one GEMM.
 inline size_t sk_part_bytes() { return (size_t)kMaxSkCtas * 2 * 128 * 16 * sizeof(float); }
-inline size_t sk_cnt_bytes(long long max_units) { return (size_t)max_units * 4 * sizeof(int); }
+inline size_t sk_cnt_bytes(int max_ctas) { return (size_t)max_ctas * 4 * sizeof(int); }
 
 // Launch attribute that lets a kernel start while the previous kernel on the stream
 // finishes (it must then call grid_dep_wait before reading that kernel's outputs).

@@ -130,7 +130,8 @@ __global__ void gather_kernel(const uint4* __restrict__ x, const int32_t* __rest
 // atomics: deterministic.  8 columns per thread.
 __global__ void combine_kernel(const float* __restrict__ ypart, const int32_t* __restrict__ ids,
                                int M, int top_k, int E, int H, uint4* __restrict__ out) {
-  grid_dep_wait();  // FC2's partial rows
+  grid_dep_wait();    // FC2's partial rows
+  grid_dep_launch();  // the stream's next kernel (the next layer's route) may be scheduled
   const int c8 = H / 8;
   const long long total = (long long)M * c8;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;

@@ -197,14 +197,23 @@ __host__ __device__ __forceinline__ int route_chunk(int P, int nwarps) {
 }
 
 // Small inputs: the whole route in one block of kWarps warps, rows in shared memory.
+// clear_words 32-bit words from err on are zeroed first (the error word and, in a
+// forward, the GEMMs' split-unit counters), so that no separate memset has to run
+// before the route.  Launched with programmatic serialization, the block waits for the
+// stream's previous kernel before touching any output, and lets the next kernel (the
+// gather) start its set-up at once.
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const int32_t* __restrict__ ids, int P, int E, int T, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ sorted_pair, int32_t* __restrict__ pair_pos,
                  int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
-                 unsigned int* __restrict__ err, int32_t* __restrict__ order, int small_rows) {
+                 unsigned int* __restrict__ err, int32_t* __restrict__ order, int small_rows,
+                 int clear_words) {
   extern __shared__ int hist[];  // [kWarps][E]
   __shared__ int scan_scratch[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int i = tid; i < clear_words; i += kRouteThreads) err[i] = 0u;
   for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
   const int chunk = route_chunk(P, kWarps);
@@ -283,18 +292,25 @@ size_t route_scratch_bytes(long long P, int E) {
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,
                          unsigned int* err, void* scratch, cudaStream_t stream, int32_t* order,
-                         int small_rows) {
+                         int small_rows, int clear_words, bool pdl) {
   const size_t smem = route_smem_bytes(E);
   const int blocks = route_blocks(P);
   if (blocks == 1) {
     cudaError_t rc = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem);
     if (rc != cudaSuccess) return rc;
-    route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, P, E, tile_n, offsets, sorted_pair,
-                                                     pair_pos, tiles, n_tiles, err, order,
-                                                     small_rows);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, route_kernel, ids, P, E, tile_n, offsets, sorted_pair,
+                              pair_pos, tiles, n_tiles, err, order, small_rows, clear_words);
   }
+  // several blocks: the caller has zeroed the error word (and any counters)
   int* gh = reinterpret_cast<int*>(scratch);
   cudaError_t rc = cudaFuncSetAttribute(route_hist_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

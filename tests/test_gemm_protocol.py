@@ -348,7 +348,8 @@ def test_stream_k_partition_and_reduction(n_units, nks, G):
     the partial slots of sk_reduce in csrc/gemm.cu), over all CTAs: every step is in
     exactly one range; a unit's pieces lie in the CTAs sk_cta_of names, in K order; the
     pieces counted by the reduction are the real ones; no CTA writes two partials into
-    one slot, and the reducer reads each CTA's partial from the slot it was written to."""
+    one slot, and the reducer reads each CTA's partial from the slot it was written to;
+    no two split units share an arrival counter (indexed by the unit's first CTA)."""
     T = n_units * nks
     starts = [_range_start(T, c, G) for c in range(G + 1)]
     assert starts[0] == 0 and starts[G] == T
@@ -367,8 +368,12 @@ def test_stream_k_partition_and_reduction(n_units, nks, G):
                 assert (c, slot) not in written, "two partials in one slot"
                 written[(c, slot)] = u
     assert len(owner) == T
+    counter_of = {}  # the reduction's counter index: the CTA holding the unit's first step
     for u, ps in pieces.items():
         c0, c1 = _cta_of(u * nks, T, G), _cta_of(u * nks + nks - 1, T, G)
+        if len(ps) > 1:
+            assert c0 not in counter_of, "two split units share an arrival counter"
+            counter_of[c0] = u
         real = [c for c, _, _ in ps]
         counted = [c for c in range(c0, c1 + 1) if starts[c + 1] > starts[c]]
         assert counted == real == sorted(real)
