@@ -55,6 +55,29 @@ def test_small_shapes_all_tokens(shape, sched):
     check_layer(li, out, layer._ws, sched, what=f"{name} sched={sched}")
 
 
+@pytest.mark.parametrize("name,sched", [("sk_m16_h1024_i2048_e16_k8", qmoe.QMOE_SCHED_DECODE),
+                                        ("sk_m1_h1024_i1024_e4_k1", qmoe.QMOE_SCHED_DECODE),
+                                        ("m300_h384_i128_e3_k2", qmoe.QMOE_SCHED_PREFILL)])
+def test_forward_needs_no_zeroed_workspace(name, sched):
+    """The forward zeroes what it needs itself (the error word and the decode schedule's
+    split-unit counters, in the route): a workspace full of garbage gives the same bits
+    as a zeroed one, and a clean error word."""
+    _, M, H, I, E, k = next(s for s in SMALL if s[0] == name)
+    li = make_inputs(LayerConfig(name, M, H, I, E, k, seed=29), "cpu").to("cuda")
+    layer = qmoe.NVFP4MoE(li.w13, li.s13, li.gs13, li.w2, li.s2, li.gs2)
+    ws = layer.workspace(M, k, sched, "cuda")
+    outs = []
+    for fill in (0x00, 0xA5, 0xFF):
+        ws.fill_(fill)
+        out = qmoe.moe_nvfp4_forward(li.x, layer.w13c, layer.w13s, layer.gs13, layer.w2c,
+                                     layer.w2s, layer.gs2, li.topk_ids, li.topk_weights,
+                                     H=H, I=I, E=E, sched=sched, workspace=ws)
+        torch.cuda.synchronize()
+        assert qmoe.qmoe_read_error(ws) == (qmoe.QMOE_OK, 0), (name, fill)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
 # Expert loads around the split prefill schedule's boundaries: tiles of up to 192 pairs,
 # those of at most 64 pairs on the decode pipeline, the rest on the prefill kernel.
 SPLIT_LOADS = [0, 1, 15, 16, 17, 63, 64, 65, 100, 128, 191, 192, 193, 256, 257, 300]
