@@ -97,8 +97,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct ForwardLayout {
   size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, route_scratch, xs, h, ypart, total;
   size_t tile_order;  // split prefill schedule: the route's two-part tile order
-  // decode schedule: arrival counters of FC1 and FC2 (cleared with the error word by one
-  // memset: [0, clear_bytes)) and the partial accumulators of split units
+  // decode schedule: arrival counters of FC1 and FC2 (cleared with the error word,
+  // [0, clear_bytes), by the one-block route or else a memset) and the partial
+  // accumulators of split units
   size_t sk_cnt1, sk_cnt2, clear_bytes, sk_part;
   int rows;  // rows of xs / h (>= 16, multiple of 16)
   int tile_n, max_tiles;
