@@ -98,8 +98,7 @@ struct ForwardLayout {
   size_t offsets, sorted_pair, pair_pos, tiles, n_tiles, route_scratch, xs, h, ypart, total;
   size_t tile_order;  // split prefill schedule: the route's two-part tile order
   // decode schedule: arrival counters of FC1 and FC2 (cleared with the error word,
-  // [0, clear_bytes), by the one-block route or else a memset) and the partial
-  // accumulators of split units
+  // [0, clear_bytes), by the route) and the partial accumulators of split units
   size_t sk_cnt1, sk_cnt2, clear_bytes, sk_part;
   int rows;  // rows of xs / h (>= 16, multiple of 16)
   int tile_n, max_tiles;
@@ -257,7 +256,7 @@ int moe_route(const int32_t* topk_ids_dev, int M, int top_k, int E, int tile_n,
   int rc = device_info(&sms);
   if (rc != QMOE_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace_dev, 0, sizeof(unsigned int), s) != cudaSuccess) return QMOE_ERR_CUDA;
+  // the route zeroes the error word itself
   return cuda_rc(launch_route(topk_ids_dev, M * top_k, E, tile_n, offsets_dev, sorted_pair_dev,
                               pair_pos_dev, tiles_dev, n_tiles_dev,
                               reinterpret_cast<unsigned int*>(workspace_dev),
@@ -370,17 +369,13 @@ static int forward_impl(const void* x_dev, const uint8_t* w13_fp4_dev, const uin
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
   };
-  // the one-block route zeroes the error word and the split-unit counters itself (and
-  // runs as a programmatic dependent of the stream's previous kernel); before the
-  // multi-block route a memset does
+  // the route zeroes the error word and the split-unit counters itself (and runs as a
+  // programmatic dependent of the stream's previous kernel)
   const bool pdl = forward_uses_pdl(rsched);
-  const bool route_clears = route_blocks(P) == 1;
-  if (!route_clears && cudaMemsetAsync(err, 0, L.clear_bytes, s) != cudaSuccess)
-    return QMOE_ERR_CUDA;
   if (!mark(0)) return QMOE_ERR_CUDA;
   cudaError_t e = launch_route(topk_ids_dev, P, E, L.tile_n, offsets, sorted_pair, pair_pos, tiles,
                                n_tiles, err, ws + L.route_scratch, s, tile_order, kSmallTileRows,
-                               (int)(L.clear_bytes / 4), pdl && route_clears);
+                               (int)(L.clear_bytes / 4), pdl);
   if (e != cudaSuccess || !mark(1)) return QMOE_ERR_CUDA;
   e = launch_gather(x_dev, pair_pos, M, top_k, H, xs, sms, s, pdl);
   if (e != cudaSuccess || !mark(2)) return QMOE_ERR_CUDA;

@@ -14,9 +14,9 @@ size_t route_smem_bytes(int E);
 size_t route_scratch_bytes(long long P, int E);
 // order (optional, needs small_rows < tile_n): the tile indices with the tiles of more
 // than small_rows pairs first, then the others; n_tiles[1] = the count of the first part
-// With one block (route_blocks(P) == 1) the kernel first zeroes clear_words 32-bit words
-// from err on; with several the caller must have zeroed the error word.  pdl: launch the
-// one-block form with programmatic stream serialization.
+// The route zeroes clear_words 32-bit words from err on (the error word and any counters
+// the caller places after it) before it raises a bad-id bit there: no memset is needed.
+// pdl: launch its kernels with programmatic stream serialization.
 int route_blocks(long long P);
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
                          int32_t* sorted_pair, int32_t* pair_pos, int32_t* tiles, int32_t* n_tiles,

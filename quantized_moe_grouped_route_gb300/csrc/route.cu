@@ -198,8 +198,8 @@ __host__ __device__ __forceinline__ int route_chunk(int P, int nwarps) {
 
 // Small inputs: the whole route in one block of kWarps warps, rows in shared memory.
 // clear_words 32-bit words from err on are zeroed first (the error word and, in a
-// forward, the GEMMs' split-unit counters), so that no separate memset has to run
-// before the route.  Launched with programmatic serialization, the block waits for the
+// forward, the GEMMs' split-unit counters), so that no memset has to run before the
+// route.  Launched with programmatic serialization, the block waits for the
 // stream's previous kernel before touching any output, and lets the next kernel (the
 // gather) start its set-up at once.
 __global__ void __launch_bounds__(kRouteThreads, 1)
@@ -229,28 +229,45 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 }
 
 // Large inputs, three kernels over `blocks` blocks of kWarps warps; the per-warp rows
-// live in global memory (gh [blocks * kWarps][E]).
+// live in global memory (gh [blocks * kWarps][E]), each block's bad-id flag in gbad
+// [blocks] after them.  The scan kernel (one block) zeroes the clear_words words from
+// err on and then raises the bad-id bit from the blocks' flags, so that no memset has to
+// run before the route.  Launched with programmatic serialization, each kernel waits
+// for its predecessor before touching any output and lets its successor be scheduled.
 __global__ void __launch_bounds__(kRouteThreads)
     route_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int* __restrict__ gh,
-                      unsigned int* __restrict__ err) {
+                      int* __restrict__ gbad) {
   extern __shared__ int hist[];  // [kWarps][E]
+  __shared__ int bad;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
+  if (tid == 0) bad = 0;
   for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
   const int chunk = route_chunk(P, gridDim.x * kWarps);
   const int lo = min(P, (blockIdx.x * kWarps + w) * chunk);
   const int hi = min(P, lo + chunk);
-  if (warp_histogram(ids, lo, hi, E, hist + w * E, lane)) atomicOr(err, QMOE_FLAG_BAD_ID);
+  if (warp_histogram(ids, lo, hi, E, hist + w * E, lane)) bad = 1;
   __syncthreads();
   int* dst = gh + (size_t)blockIdx.x * kWarps * E;
   for (int i = tid; i < kWarps * E; i += kRouteThreads) dst[i] = hist[i];
+  if (tid == 0) gbad[blockIdx.x] = bad;
 }
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_scan_kernel(int R, int E, int T, int* __restrict__ gh, int32_t* __restrict__ offsets,
                       int32_t* __restrict__ tiles, int32_t* __restrict__ n_tiles,
-                      int32_t* __restrict__ order, int small_rows) {
+                      int32_t* __restrict__ order, int small_rows, const int* __restrict__ gbad,
+                      int nblocks, unsigned int* __restrict__ err, int clear_words) {
   __shared__ int scan_scratch[kWarps];
+  const int tid = threadIdx.x;
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int i = tid; i < clear_words; i += kRouteThreads) err[i] = 0u;
+  int any = 0;
+  for (int b = tid; b < nblocks; b += kRouteThreads) any |= gbad[b];
+  if (__syncthreads_or(any) && tid == 0) atomicOr(err, QMOE_FLAG_BAD_ID);
   route_scan(gh, R, E, T, offsets, tiles, n_tiles, scan_scratch, order, small_rows);
 }
 
@@ -260,6 +277,8 @@ __global__ void __launch_bounds__(kRouteThreads)
                          int32_t* __restrict__ pair_pos) {
   extern __shared__ int hist[];  // [kWarps][E]: this block's warps' first positions
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
   const int* src = gh + (size_t)blockIdx.x * kWarps * E;
   for (int i = tid; i < kWarps * E; i += kRouteThreads) hist[i] = src[i];
   __syncthreads();
@@ -286,7 +305,7 @@ int route_blocks(long long P) {
 
 size_t route_scratch_bytes(long long P, int E) {
   const int b = route_blocks(P);
-  return b > 1 ? (size_t)b * kWarps * (size_t)E * sizeof(int) : 0;
+  return b > 1 ? (size_t)b * (kWarps * (size_t)E + 1) * sizeof(int) : 0;
 }
 
 cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* offsets,
@@ -310,20 +329,33 @@ cudaError_t launch_route(const int32_t* ids, int P, int E, int tile_n, int32_t* 
     return cudaLaunchKernelEx(&cfg, route_kernel, ids, P, E, tile_n, offsets, sorted_pair,
                               pair_pos, tiles, n_tiles, err, order, small_rows, clear_words);
   }
-  // several blocks: the caller has zeroed the error word (and any counters)
   int* gh = reinterpret_cast<int*>(scratch);
+  int* gbad = gh + (size_t)blocks * kWarps * E;
   cudaError_t rc = cudaFuncSetAttribute(route_hist_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc == cudaSuccess)
     rc = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem);
   if (rc != cudaSuccess) return rc;
-  route_hist_kernel<<<blocks, kRouteThreads, smem, stream>>>(ids, P, E, gh, err);
-  route_scan_kernel<<<1, kRouteThreads, 0, stream>>>(blocks * kWarps, E, tile_n, gh, offsets, tiles,
-                                                     n_tiles, order, small_rows);
-  route_scatter_kernel<<<blocks, kRouteThreads, smem, stream>>>(ids, P, E, gh, offsets, sorted_pair,
-                                                                pair_pos);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.gridDim = dim3(blocks);
+  cfg.dynamicSmemBytes = smem;
+  rc = cudaLaunchKernelEx(&cfg, route_hist_kernel, ids, P, E, gh, gbad);
+  if (rc != cudaSuccess) return rc;
+  cfg.gridDim = dim3(1);
+  cfg.dynamicSmemBytes = 0;
+  rc = cudaLaunchKernelEx(&cfg, route_scan_kernel, blocks * kWarps, E, tile_n, gh, offsets, tiles,
+                          n_tiles, order, small_rows, (const int*)gbad, blocks, err, clear_words);
+  if (rc != cudaSuccess) return rc;
+  cfg.gridDim = dim3(blocks);
+  cfg.dynamicSmemBytes = smem;
+  return cudaLaunchKernelEx(&cfg, route_scatter_kernel, ids, P, E, (const int*)gh,
+                            (const int32_t*)offsets, sorted_pair, pair_pos);
 }
 
 }  // namespace qmoe

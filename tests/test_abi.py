@@ -34,7 +34,8 @@ def test_size_queries(lib):
     assert qmoe.qmoe_sched_tile_n(qmoe.QMOE_SCHED_PREFILL_PAIR, 8192, 8, 256) == 256
     # above 8192 pairs the route keeps per-warp count tables in its workspace
     assert qmoe.qmoe_route_workspace_size(1024, 8, 256, 320) == 256
-    assert qmoe.qmoe_route_workspace_size(8192, 8, 256, 320) == 256 + 16 * 16 * 256 * 4
+    # the multi-block route's per-warp count tables and one bad-id flag per block
+    assert qmoe.qmoe_route_workspace_size(8192, 8, 256, 320) == 256 + 16 * (16 * 256 + 1) * 4
     # kernels per forward: route (one, or three above 8192 pairs), gather, FC1, FC2, combine
     assert qmoe.qmoe_forward_kernel_count(16, 8, 256, qmoe.QMOE_SCHED_AUTO) == 5
     assert qmoe.qmoe_forward_kernel_count(8192, 8, 256, qmoe.QMOE_SCHED_AUTO) == 7
