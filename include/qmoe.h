@@ -154,7 +154,9 @@ int moe_nvfp4_repack(const uint8_t* w_fp4_dev, const uint8_t* w_scale_dev, int E
  *   sched           QMOE_SCHED_*
  *   workspace_dev   >= qmoe_forward_workspace_size(M, H, I, E, top_k, sched) bytes,
  *                   256-byte aligned; holds the error word, routing tables, the
- *                   gathered activations, h and the per-pair partial outputs.
+ *                   gathered activations, h and the per-pair partial outputs.  Its
+ *                   contents on entry do not matter: the call zeroes what it needs
+ *                   (the error word and the decode schedule's counters) itself.
  * Deterministic: two calls on the same inputs give bitwise equal outputs.  Calls
  * sharing one workspace must not overlap on the GPU.
  */
