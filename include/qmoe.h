@@ -200,7 +200,7 @@ int moe_nvfp4_forward_limit(const void* x_dev, const uint8_t* w13_fp4_dev,
  * library, which every GPU that loads the library holds until the process exits.
  *  - Size limit: the batch must fit that array, i.e. qmoe_forward_workspace_size(
  *    M, H, I, E, top_k, sched) <= QMOE_NOALLOC_SCRATCH_BYTES (decode-sized batches:
- *    e.g. M = 16, H = 7168, I = 2048, top_k = 8 needs about 6 MB); larger batches get
+ *    e.g. M = 16, H = 7168, I = 2048, top_k = 8 needs about 9 MB); larger batches get
  *    QMOE_ERR_WORKSPACE before anything is enqueued.
  *  - Set-up: the array's device address is looked up (cudaGetSymbolAddress) on the
  *    first call made on a device, and again whenever a call finds another CUDA context
