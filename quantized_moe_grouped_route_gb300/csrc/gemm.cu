@@ -1,7 +1,7 @@
 // Persistent grouped GEMM for FC1 (+ SwiGLU) and FC2 (+ global scale and routing
 // weight) of the NVFP4 W4A16 MoE layer, on tcgen05 tensor cores.
 //
-// What it computes (megamoe_rm.cu page, fc1_rm / fc2_rm; spec layer):
+// What it computes (megamoe_rm.cu page, fc1_rm / fc2_rm):
 //   FC1 tile (expert e, 128 weight rows rb, pair tile t):
 //     g = gs13[e] * Wq13[e][rows] . xs[t]^T, then h = bf16(SiLU(gate) * up), with
 //     the GLM clamp of gate and up first when a SwiGLU limit is given (CLAMP)
